@@ -1,0 +1,20 @@
+"""Plain fp64 CPU oracle for SnapKV observation-window KV selection.
+
+Test infrastructure only: tests/, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.
+The product path (the CUDA library and its Python binding) never does.
+"""
+
+from .snapkv_oracle import (  # noqa: F401
+    OracleArgumentError,
+    causal_probabilities,
+    check_head_args,
+    pool_scores,
+    prefix_votes,
+    select_from_pooled,
+    snapkv_head,
+    snapkv_packed,
+    top_prefix,
+    window_logits,
+    window_row_exp_sums,
+)
