@@ -1,0 +1,184 @@
+/*
+ * kvsel.h — C ABI of libkvsel, GB300 (sm_103a) SnapKV observation-window
+ * KV-cache selection.
+ *
+ * Method: page "SnapKV: choosing the KV cache of a long prompt with an
+ * observation window" (SnapKV：用观察窗口为长提示词选择 KV Cache,
+ * charlestar.github.io, 2026-10-20). For every (layer, sequence, head):
+ *   - partition ("要缩小的是提示词缓存" section): prompt length L, window = the
+ *     last W tokens, prefix P = L - W, budget C keeps the whole window plus
+ *     C - W prefix positions;
+ *   - votes ("投票必须来自完整提示词的因果 softmax" section): the W window
+ *     queries attend to all L keys with scale 1/sqrt(D) under a causal mask,
+ *     the softmax denominator runs over every visible position, and each
+ *     prefix position's vote is the sum of its probabilities over the W rows;
+ *   - pooling and top-k ("池化把一个峰值扩展成邻域偏好" section): 1-D pooling
+ *     of the prefix votes (odd width, stride 1, zero padding; the average
+ *     divides by the full width at the edges; or max), then the C - W prefix
+ *     positions with the highest pooled score, ties to the smaller position;
+ *   - gather ("从 Q 和 K 开始算一次完整选择" section): the kept positions of
+ *     K and V with one index list; L < C keeps everything (bypass).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Data layout (row-major, no padding, "layers" outermost):
+ *   q_win   [num_layers][num_seqs * W][H][D]  window queries; rows b*W .. b*W+W-1
+ *                                             are sequence b's positions P_b .. L_b-1
+ *   K, V    [num_layers][T][H][D]             packed prompts (RoPE already applied);
+ *                                             sequence b owns tokens
+ *                                             seq_offsets[b] .. seq_offsets[b+1]-1
+ *   votes, pooled [num_layers][H][T] fp32     entry j of sequence b's token range holds
+ *                                             prefix position j's score (j < P_b); window
+ *                                             positions hold 0
+ *   out_idx [num_layers][T_out][H] int32      positions within the sequence
+ *   out_K, out_V [num_layers][T_out][H][D]    same dtype as K and V
+ * with T = seq_offsets[num_seqs] and T_out = kvsel_out_tokens(shape, C)
+ * = sum_b min(L_b, C); sequence b's output rows start at sum_{b'<b} min(L_b', C).
+ * Within a sequence's C output rows: the C - W kept prefix positions in the
+ * order (highest pooled score first, equal scores by smaller position), then
+ * the window positions P..L-1 ascending. A sequence with L < C (bypass) keeps
+ * positions 0..L-1 in order.
+ *
+ * Memory: every data pointer is device memory allocated by the caller, except
+ * shape->seq_offsets, which is HOST memory (it decides launch shapes and which
+ * sequences bypass). The library never frees caller memory.
+ *
+ * Streams and synchronisation: `stream` is a cudaStream_t (NULL = legacy
+ * default stream). Calls enqueue work and return without waiting for it.
+ * kvsel_score, kvsel_window_logits and kvsel_snapkv use an internal per-device
+ * workspace that the library allocates with cudaMalloc and grows on demand
+ * (growing synchronises the device); kvsel_release() frees it. Calls that use
+ * the workspace on one device must be ordered with one another (one stream,
+ * or events between streams): overlapping calls race on it.
+ *
+ * Errors: arguments are checked on the host before any launch; a rejected
+ * call launches nothing. Conditions only the GPU can see (a non-finite window
+ * logit, a gather index out of range, a bounded wait that ran out) are
+ * recorded in a per-device status word; kvsel_device_status() reads it.
+ * Every launch failure returns KVSEL_ERR_CUDA.
+ */
+#ifndef KVSEL_H_
+#define KVSEL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kvsel_status;
+enum {
+  KVSEL_OK = 0,
+  KVSEL_ERR_INVALID_ARG = 1,  /* an argument rule failed (see each call) */
+  KVSEL_ERR_UNSUPPORTED = 2,  /* valid, but beyond a documented limit */
+  KVSEL_ERR_NONFINITE = 3,    /* device: a window logit was NaN or +-Inf */
+  KVSEL_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out */
+  KVSEL_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  KVSEL_ERR_BAD_INDEX = 6     /* device: a gather index was outside [0, L_b) */
+};
+
+enum { KVSEL_POOL_AVG = 0, KVSEL_POOL_MAX = 1 };
+enum { KVSEL_BF16 = 0, KVSEL_F32 = 1 };
+
+/* Shape of one call. num_layers >= 1 and num_heads >= 1 and head_dim >= 1;
+ * num_seqs >= 0 (0 = nothing to do); dtype is KVSEL_BF16 or KVSEL_F32 (for
+ * q_win, K, V and the gathered outputs). seq_offsets: HOST array of
+ * num_seqs + 1 entries, seq_offsets[0] == 0, nondecreasing. */
+typedef struct kvsel_shape {
+  int32_t num_layers;
+  int32_t num_seqs;
+  int32_t num_heads;
+  int32_t head_dim;
+  int32_t dtype;
+  int32_t reserved; /* must be 0 */
+  const int64_t* seq_offsets;
+} kvsel_shape;
+
+/* Library version string (static storage). */
+const char* kvsel_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* kvsel_status_string(kvsel_status status);
+
+/* T_out = sum_b min(L_b, C), the number of output rows per layer and head.
+ * Returns -1 if the shape or C (< 1) is invalid. Host only, no GPU work. */
+int64_t kvsel_out_tokens(const kvsel_shape* shape, int32_t C);
+
+/* Which window-logit kernel a call with this shape takes: 1 = the tensor-core
+ * kernel (TMA + tcgen05, bf16, D in {64,128}, W <= 64), 0 = the CUDA-core
+ * kernel (any other supported shape), -1 = the call would be rejected.
+ * C = 0 means "score every sequence" (kvsel_score); otherwise sequences with
+ * L < C are not scored. Host only; queries the current device. */
+int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C);
+
+/* Window logits z[r][j] = q_{P_b + r} . k_j / sqrt(D) for every sequence b,
+ * window row r < W and token j of b (no mask applied), written to
+ * logits[num_layers][H][W][T] (fp32, row r of column j belongs to j's
+ * sequence). Rules: W >= 1, W <= L_b for every b, non-null pointers when
+ * T > 0. Same kernels as kvsel_score, stopped before the softmax; for tests
+ * and diagnostics. */
+kvsel_status kvsel_window_logits(const kvsel_shape* shape, const void* q_win, const void* K,
+                                 int32_t W, float* logits, void* stream);
+
+/* Votes and pooled scores of every sequence ("votes" and "pooling" sections).
+ * votes (may be NULL) and pooled: [num_layers][H][T] fp32, prefix positions
+ * filled, window positions 0. Rules: W >= 1, W <= L_b for every b, pool_kind
+ * in {AVG, MAX}, pool_k odd and >= 1, non-null q_win/K/pooled when T > 0.
+ * Device status: NONFINITE if a window logit (any window row, any token of
+ * the sequence) is not finite. */
+kvsel_status kvsel_score(const kvsel_shape* shape, const void* q_win, const void* K, int32_t W,
+                         int32_t pool_kind, int32_t pool_k, float* votes, float* pooled,
+                         void* stream);
+
+/* Top-(C - W) selection from given pooled scores ([num_layers][H][T] fp32,
+ * only prefix entries are read) into out_idx ([num_layers][T_out][H] int32);
+ * bypass sequences (L < C) get 0..L-1. Ordering of scores: IEEE order with
+ * -0 == +0; NaN ranks below every number and sets NONFINITE. Rules: W >= 1,
+ * C > W, W <= L_b for every b. Limit: C - W <= 16384 (else UNSUPPORTED). */
+kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t W, int32_t C,
+                          int32_t* out_idx, void* stream);
+
+/* Gather: out_K[row] = K[idx], out_V[row] = V[idx] for every output row, the
+ * same idx for K and V, with out_idx as produced by kvsel_select. Rules: C >= 1,
+ * non-null pointers when T_out > 0. Device status: BAD_INDEX if an index is
+ * outside [0, L_b) (that row is left unwritten). Bit-exact copy. */
+kvsel_status kvsel_compact(const kvsel_shape* shape, const void* K, const void* V,
+                           const int32_t* out_idx, int32_t C, void* out_K, void* out_V,
+                           void* stream);
+
+/* The whole path: score -> pool -> select -> gather, with no host
+ * synchronisation in between. Rules: those of kvsel_score and kvsel_select
+ * (W >= 1, C > W, W <= L_b for every b, odd pool_k >= 1, pool_kind valid,
+ * C - W <= 16384). Sequences with L < C are copied unscored. */
+kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const void* K,
+                          const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                          int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                          void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: the first device-side error recorded since the last call, or
+ * KVSEL_OK. Returns KVSEL_ERR_CUDA if the synchronisation itself failed. */
+kvsel_status kvsel_device_status(void* stream);
+
+/* Upper bound, in nanoseconds, on every spin-wait inside the kernels (default
+ * 2e9). A wait that runs out records KVSEL_ERR_TIMEOUT and the kernel skips
+ * the dependent work and exits normally. Must be >= 1000. */
+kvsel_status kvsel_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the bounded waits. what = 1: the next tensor-core scoring
+ * launch withholds the row statistics of its first work item, so the other
+ * work items of that (layer, sequence, head) wait until the limit and report
+ * KVSEL_ERR_TIMEOUT. what = 0 clears it. */
+kvsel_status kvsel_debug_inject(int32_t what);
+
+/* Frees the internal workspace of every device this process used. Calls
+ * still running on the GPU must have finished (the call synchronises each
+ * device first). */
+void kvsel_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVSEL_H_ */

@@ -1,0 +1,228 @@
+"""Thin Python binding of libkvsel: the C ABI's names, torch tensors in and out.
+
+Argument marshalling only: every step of the selection runs in the library's
+CUDA kernels. Tensors must be CUDA, contiguous, and laid out as ``kvsel.h``
+states:
+
+    q_win  [layers, S*W, H, D]      K, V  [layers, T, H, D]      (bf16 or fp32)
+    votes, pooled [layers, H, T] fp32
+    out_idx [layers, T_out, H] int32     out_K, out_V [layers, T_out, H, D]
+
+3-D tensors (no layer axis) are accepted as one layer. ``seq_offsets`` is a
+host sequence of S + 1 token offsets. Work is queued on the current torch
+stream (or ``stream``); call ``kvsel_device_status`` to learn about errors
+only the GPU can see.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import _native
+
+KVSEL_OK = 0
+KVSEL_ERR_INVALID_ARG = 1
+KVSEL_ERR_UNSUPPORTED = 2
+KVSEL_ERR_NONFINITE = 3
+KVSEL_ERR_TIMEOUT = 4
+KVSEL_ERR_CUDA = 5
+KVSEL_ERR_BAD_INDEX = 6
+KVSEL_POOL_AVG = 0
+KVSEL_POOL_MAX = 1
+KVSEL_BF16 = 0
+KVSEL_F32 = 1
+
+_DTYPES = {torch.bfloat16: KVSEL_BF16, torch.float32: KVSEL_F32}
+
+
+class KvselError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kvsel_status_string(status)} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != KVSEL_OK:
+        raise KvselError(status, where)
+
+
+def kvsel_version() -> str:
+    return _native.lib().kvsel_version().decode()
+
+
+def kvsel_status_string(status: int) -> str:
+    return _native.lib().kvsel_status_string(int(status)).decode()
+
+
+class Shape:
+    """Builds a ``kvsel_shape`` and keeps its host offsets alive."""
+
+    def __init__(self, num_layers: int, num_heads: int, head_dim: int, dtype: int,
+                 seq_offsets: Sequence[int]):
+        offs = [int(x) for x in seq_offsets]
+        self._offs = (ctypes.c_int64 * max(1, len(offs)))(*offs)
+        self.c = _native.KvselShape(int(num_layers), len(offs) - 1, int(num_heads),
+                                    int(head_dim), int(dtype), 0,
+                                    ctypes.cast(self._offs, ctypes.POINTER(ctypes.c_int64)))
+        self.T = offs[-1] if offs else 0
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def _as4(t: torch.Tensor) -> torch.Tensor:
+    return t.unsqueeze(0) if t.dim() == 3 else t
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+
+
+def shape_of(K: torch.Tensor, seq_offsets: Sequence[int]) -> Shape:
+    K4 = _as4(K)
+    if K4.dtype not in _DTYPES:
+        raise ValueError("K must be bf16 or fp32")
+    return Shape(K4.shape[0], K4.shape[2], K4.shape[3], _DTYPES[K4.dtype], seq_offsets)
+
+
+def kvsel_out_tokens(shape: Shape, C: int) -> int:
+    return int(_native.lib().kvsel_out_tokens(shape.ref, int(C)))
+
+
+def kvsel_score_path(shape: Shape, W: int, C: int = 0) -> int:
+    return int(_native.lib().kvsel_score_path(shape.ref, int(W), int(C)))
+
+
+def kvsel_window_logits(q_win, K, seq_offsets, W: int, logits=None, stream=None):
+    """Raw window logits [layers, H, W, T] fp32 (diagnostic)."""
+    sh = shape_of(K, seq_offsets)
+    K4, q4 = _as4(K), _as4(q_win)
+    _need(K4, "K"), _need(q4, "q_win", K4.dtype)
+    L, _, H, _ = K4.shape
+    if logits is None:
+        logits = torch.empty((L, H, int(W), sh.T), dtype=torch.float32, device=K.device)
+    _need(logits, "logits", torch.float32)
+    _check(_native.lib().kvsel_window_logits(sh.ref, _ptr(q4), _ptr(K4), int(W), _ptr(logits),
+                                             _stream(stream)), "kvsel_window_logits")
+    return logits
+
+
+def kvsel_score(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: int,
+                votes=None, pooled=None, want_votes: bool = True, stream=None):
+    """(votes, pooled), each [layers, H, T] fp32; votes is None if not wanted."""
+    sh = shape_of(K, seq_offsets)
+    K4, q4 = _as4(K), _as4(q_win)
+    _need(K4, "K"), _need(q4, "q_win", K4.dtype)
+    L, _, H, _ = K4.shape
+    if votes is None and want_votes:
+        votes = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
+    if pooled is None:
+        pooled = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
+    for t, n in ((votes, "votes"), (pooled, "pooled")):
+        if t is not None:
+            _need(t, n, torch.float32)
+    _check(_native.lib().kvsel_score(sh.ref, _ptr(q4), _ptr(K4), int(W), int(pool_kind),
+                                     int(pool_k), _ptr(votes), _ptr(pooled), _stream(stream)),
+           "kvsel_score")
+    return votes, pooled
+
+
+def kvsel_select(pooled, seq_offsets, num_heads: int, W: int, C: int, out_idx=None,
+                 stream=None):
+    """out_idx [layers, T_out, H] int32 from pooled scores [layers, H, T]."""
+    p3 = pooled if pooled.dim() == 3 else pooled.unsqueeze(0)
+    _need(p3, "pooled", torch.float32)
+    L = p3.shape[0]
+    sh = Shape(L, num_heads, 1, KVSEL_F32, seq_offsets)
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_select")
+    if out_idx is None:
+        out_idx = torch.empty((L, t_out, num_heads), dtype=torch.int32, device=pooled.device)
+    _need(out_idx, "out_idx", torch.int32)
+    _check(_native.lib().kvsel_select(sh.ref, _ptr(p3), int(W), int(C), _ptr(out_idx),
+                                      _stream(stream)), "kvsel_select")
+    return out_idx
+
+
+def kvsel_compact(K, V, seq_offsets, out_idx, C: int, out_K=None, out_V=None, stream=None):
+    """(out_K, out_V) [layers, T_out, H, D] gathered with out_idx."""
+    sh = shape_of(K, seq_offsets)
+    K4, V4 = _as4(K), _as4(V)
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(out_idx, "out_idx", torch.int32)
+    L, _, H, D = K4.shape
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_compact")
+    if out_K is None:
+        out_K = torch.empty((L, t_out, H, D), dtype=K.dtype, device=K.device)
+    if out_V is None:
+        out_V = torch.empty((L, t_out, H, D), dtype=K.dtype, device=K.device)
+    _need(out_K, "out_K", K4.dtype), _need(out_V, "out_V", K4.dtype)
+    _check(_native.lib().kvsel_compact(sh.ref, _ptr(K4), _ptr(V4), _ptr(out_idx), int(C),
+                                       _ptr(out_K), _ptr(out_V), _stream(stream)),
+           "kvsel_compact")
+    return out_K, out_V
+
+
+def kvsel_snapkv(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int, pool_k: int,
+                 out_idx=None, out_K=None, out_V=None, stream=None
+                 ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """The fused path: (out_idx, out_K, out_V)."""
+    sh = shape_of(K, seq_offsets)
+    K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q_win", K4.dtype)
+    L, _, H, D = K4.shape
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_snapkv")
+    dev = K.device
+    if out_idx is None:
+        out_idx = torch.empty((L, t_out, H), dtype=torch.int32, device=dev)
+    if out_K is None:
+        out_K = torch.empty((L, t_out, H, D), dtype=K.dtype, device=dev)
+    if out_V is None:
+        out_V = torch.empty((L, t_out, H, D), dtype=K.dtype, device=dev)
+    _need(out_idx, "out_idx", torch.int32)
+    _need(out_K, "out_K", K4.dtype), _need(out_V, "out_V", K4.dtype)
+    _check(_native.lib().kvsel_snapkv(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W), int(C),
+                                      int(pool_kind), int(pool_k), _ptr(out_idx), _ptr(out_K),
+                                      _ptr(out_V), _stream(stream)), "kvsel_snapkv")
+    return out_idx, out_K, out_V
+
+
+def kvsel_device_status(stream=None) -> int:
+    return int(_native.lib().kvsel_device_status(_stream(stream)))
+
+
+def kvsel_set_wait_limit_ns(ns: int) -> None:
+    _check(_native.lib().kvsel_set_wait_limit_ns(int(ns)), "kvsel_set_wait_limit_ns")
+
+
+def kvsel_debug_inject(what: int) -> None:
+    _check(_native.lib().kvsel_debug_inject(int(what)), "kvsel_debug_inject")
+
+
+def kvsel_release() -> None:
+    _native.lib().kvsel_release()

@@ -1,0 +1,602 @@
+// libkvsel C ABI: argument rules, per-call planning, the per-device workspace
+// and status word, and the launch sequence of each entry point.
+//
+// Argument rules follow the page "SnapKV: choosing the KV cache of a long
+// prompt with an observation window", section "Computing one full selection
+// from Q and K" (从 Q 和 K 开始算一次完整选择): positive integer window,
+// capacity and kernel, W <= L, C > W, odd kernel, avg or max pooling; a
+// prompt shorter than the budget bypasses selection (L == C runs the normal
+// path).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kvsel_internal.h"
+
+namespace kvsel {
+
+__device__ int g_status_word;  // first device-side error of the current device
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;        // device address of g_status_word
+  char* ws = nullptr;           // workspace
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+unsigned long long g_wait_limit_ns = 2000000000ull;
+int g_inject = 0;
+
+kvsel_status cuda_fail(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KVSEL_OK;
+  std::fprintf(stderr, "libkvsel: %s failed: %s\n", what, cudaGetErrorString(e));
+  return KVSEL_ERR_CUDA;
+}
+
+kvsel_status device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVSEL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_status_word)))
+      return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    d.status = static_cast<int*>(p);
+    if ((e = cudaMemset(d.status, 0, sizeof(int)))) return cuda_fail(e, "cudaMemset(status)");
+    d.ready = true;
+  }
+  *out = &d;
+  return KVSEL_OK;
+}
+
+// Grows the device workspace to at least `bytes` (synchronising the device
+// before freeing the old one, which queued work may still use).
+kvsel_status workspace(DevState* d, size_t bytes, char** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (bytes > d->ws_bytes) {
+    cudaError_t e;
+    if (d->ws) {
+      if ((e = cudaDeviceSynchronize())) return cuda_fail(e, "cudaDeviceSynchronize");
+      cudaFree(d->ws);
+      d->ws = nullptr;
+      d->ws_bytes = 0;
+    }
+    size_t want = (bytes + (1u << 20) - 1) & ~size_t((1u << 20) - 1);
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&d->ws), want)))
+      return cuda_fail(e, "cudaMalloc(workspace)");
+    d->ws_bytes = want;
+  }
+  *out = d->ws;
+  return KVSEL_OK;
+}
+
+// Bump allocator over the workspace (256-byte aligned pieces).
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t at = off;
+    off += (bytes + 255) & ~size_t(255);
+    return at;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Argument rules and the per-call plan
+// ---------------------------------------------------------------------------
+
+struct Plan {
+  int layers = 0, S = 0, H = 0, D = 0, dtype = 0;
+  int64_t T = 0, T_out = 0;
+  int elem_bytes = 0;
+  std::vector<SeqDesc> all;      // every sequence
+  int min_len = 0;
+};
+
+kvsel_status plan_shape(const kvsel_shape* sh, int C, Plan* p) {
+  if (!sh) return KVSEL_ERR_INVALID_ARG;
+  if (sh->num_layers < 1 || sh->num_seqs < 0 || sh->num_heads < 1 || sh->head_dim < 1 ||
+      sh->reserved != 0)
+    return KVSEL_ERR_INVALID_ARG;
+  if (sh->dtype != KVSEL_BF16 && sh->dtype != KVSEL_F32) return KVSEL_ERR_INVALID_ARG;
+  if (sh->num_seqs > 0 && !sh->seq_offsets) return KVSEL_ERR_INVALID_ARG;
+  p->layers = sh->num_layers;
+  p->S = sh->num_seqs;
+  p->H = sh->num_heads;
+  p->D = sh->head_dim;
+  p->dtype = sh->dtype;
+  p->elem_bytes = sh->dtype == KVSEL_BF16 ? 2 : 4;
+  p->all.clear();
+  p->min_len = 0x7fffffff;
+  if (p->S == 0) {
+    p->min_len = 0;
+    return KVSEL_OK;
+  }
+  if (sh->seq_offsets[0] != 0) return KVSEL_ERR_INVALID_ARG;
+  int64_t out = 0;
+  for (int b = 0; b < p->S; ++b) {
+    const int64_t a0 = sh->seq_offsets[b], a1 = sh->seq_offsets[b + 1];
+    if (a1 < a0) return KVSEL_ERR_INVALID_ARG;
+    if (a1 - a0 > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+    SeqDesc s{};
+    s.tok_off = a0;
+    s.len = (int32_t)(a1 - a0);
+    s.out_off = (int32_t)out;
+    s.index = b;
+    if (C > 0) out += s.len < C ? s.len : C;
+    if (out > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+    p->all.push_back(s);
+    if (s.len < p->min_len) p->min_len = s.len;
+  }
+  p->T = sh->seq_offsets[p->S];
+  p->T_out = out;
+  const double elems = (double)p->layers * (double)p->T * p->H * p->D;
+  if (elems > 4.0e18 || p->T > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+  return KVSEL_OK;
+}
+
+kvsel_status check_window(const Plan& p, int W) {
+  if (W < 1) return KVSEL_ERR_INVALID_ARG;
+  for (const SeqDesc& s : p.all)
+    if (W > s.len) return KVSEL_ERR_INVALID_ARG;
+  return KVSEL_OK;
+}
+
+kvsel_status check_pool(int kind, int k) {
+  if (kind != KVSEL_POOL_AVG && kind != KVSEL_POOL_MAX) return KVSEL_ERR_INVALID_ARG;
+  if (k < 1 || (k % 2) != 1) return KVSEL_ERR_INVALID_ARG;
+  return KVSEL_OK;
+}
+
+kvsel_status check_budget(int W, int C) {
+  if (C <= W) return KVSEL_ERR_INVALID_ARG;
+  if (C - W > kMaxSelect) return KVSEL_ERR_UNSUPPORTED;
+  return KVSEL_OK;
+}
+
+bool gen_supported(int W, int D) { return (int64_t)W * D <= kGenericMaxQ; }
+
+// Scoring plan: the scored sequences (all when C == 0, else L >= C) with
+// their work-item and instance numbering for the chosen kernel.
+struct ScorePlan {
+  bool tc = false;
+  int chunk = 0, wpad = 0;
+  std::vector<SeqDesc> scored;
+  int items_per_layer = 0, inst_per_layer = 0, max_chunks = 0;
+};
+
+kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* k,
+                        const DevState* d, ScorePlan* sp) {
+  const bool tc_ok = d->cc_major == 10 && tc_eligible(p.dtype, p.D, W, q, k);
+  auto build = [&](int chunk) {
+    sp->scored.clear();
+    sp->items_per_layer = sp->inst_per_layer = sp->max_chunks = 0;
+    for (const SeqDesc& s0 : p.all) {
+      if (C > 0 && s0.len < C) continue;
+      SeqDesc s = s0;
+      s.n_chunks = (s.len + chunk - 1) / chunk;
+      if (s.n_chunks == 0) continue;  // empty sequence (W <= 0 already rejected)
+      s.item_base = sp->items_per_layer;
+      s.inst_base = sp->inst_per_layer;
+      sp->items_per_layer += p.H * s.n_chunks;
+      sp->inst_per_layer += p.H;
+      if (s.n_chunks > sp->max_chunks) sp->max_chunks = s.n_chunks;
+      sp->scored.push_back(s);
+    }
+  };
+  if (tc_ok) {
+    build(tc_chunk_tokens(W));
+    // every chunk of one instance must be resident at once (one CTA per SM)
+    if (sp->max_chunks <= tc_max_grid(d->sm_count)) {
+      sp->tc = true;
+      sp->chunk = tc_chunk_tokens(W);
+      sp->wpad = tc_window_pad(W);
+      return KVSEL_OK;
+    }
+  }
+  if (!gen_supported(W, p.D)) return KVSEL_ERR_UNSUPPORTED;
+  sp->tc = false;
+  sp->chunk = kGenericChunk;
+  sp->wpad = W;
+  build(kGenericChunk);
+  return KVSEL_OK;
+}
+
+// Uploads the sequence tables and runs the scoring kernels (votes or logits).
+kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const void* q,
+                       const void* k, int W, float* votes, float* logits, char* ws,
+                       Carve& cv, cudaStream_t stream) {
+  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
+  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
+  if (items == 0) return KVSEL_OK;
+  if (items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+  const size_t o_seq = cv.take(sp.scored.size() * sizeof(SeqDesc));
+  const size_t o_part = cv.take((size_t)items * sp.wpad * 2 * sizeof(float));
+  const size_t o_cnt = cv.take((size_t)insts * 2 * sizeof(int));
+  const size_t o_fin = cv.take((size_t)insts * sp.wpad * sizeof(float));
+  cudaError_t e = cudaMemcpyAsync(ws + o_seq, sp.scored.data(),
+                                  sp.scored.size() * sizeof(SeqDesc),
+                                  cudaMemcpyHostToDevice, stream);
+  if (e) return cuda_fail(e, "cudaMemcpyAsync(sequence table)");
+  ScoreArgs a{};
+  a.q = q;
+  a.k = k;
+  a.layers = p.layers;
+  a.H = p.H;
+  a.D = p.D;
+  a.dtype = p.dtype;
+  a.W = W;
+  a.T = p.T;
+  a.q_rows = (int64_t)p.S * W;
+  a.n_scored = (int)sp.scored.size();
+  a.seqs = reinterpret_cast<const SeqDesc*>(ws + o_seq);
+  a.items_per_layer = sp.items_per_layer;
+  a.inst_per_layer = sp.inst_per_layer;
+  a.chunk_tokens = sp.chunk;
+  a.wpad = sp.wpad;
+  a.scale = (float)(1.0 / std::sqrt((double)p.D));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
+  a.part = reinterpret_cast<float*>(ws + o_part);
+  a.counters = reinterpret_cast<int*>(ws + o_cnt);
+  a.flags = a.counters + insts;
+  a.final_stats = reinterpret_cast<float*>(ws + o_fin);
+  a.votes = votes;
+  a.logits = logits;
+  a.status = d->status;
+  a.sm_count = d->sm_count;
+  a.stream = stream;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_limit_ns = g_wait_limit_ns;
+    a.inject = g_inject;
+    if (sp.tc && logits == nullptr) g_inject = 0;  // one-shot
+  }
+  if (sp.tc) {
+    if ((e = cudaMemsetAsync(a.counters, 0, (size_t)insts * 2 * sizeof(int), stream)))
+      return cuda_fail(e, "cudaMemsetAsync(counters)");
+    int grid = tc_max_grid(d->sm_count);
+    if (items < grid) grid = (int)items;
+    e = launch_tc_score(a, logits != nullptr, grid);
+    return cuda_fail(e, "tensor-core scoring launch");
+  }
+  e = launch_generic_score(a, logits != nullptr);
+  return cuda_fail(e, "CUDA-core scoring launch");
+}
+
+kvsel_status upload_all(const Plan& p, char* ws, Carve& cv, cudaStream_t stream,
+                        const SeqDesc** out) {
+  const size_t o = cv.take(p.all.size() * sizeof(SeqDesc) + 1);
+  cudaError_t e = cudaMemcpyAsync(ws + o, p.all.data(), p.all.size() * sizeof(SeqDesc),
+                                  cudaMemcpyHostToDevice, stream);
+  if (e) return cuda_fail(e, "cudaMemcpyAsync(sequence table)");
+  *out = reinterpret_cast<const SeqDesc*>(ws + o);
+  return KVSEL_OK;
+}
+
+size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
+  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
+  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
+  return 4096 + sp.scored.size() * sizeof(SeqDesc) + (size_t)items * sp.wpad * 8 +
+         (size_t)insts * 8 + (size_t)insts * sp.wpad * 4 + 4 * 256;
+}
+
+}  // namespace
+}  // namespace kvsel
+
+using namespace kvsel;
+
+extern "C" {
+
+const char* kvsel_version(void) { return "kvsel 0.1.0 (sm_103a)"; }
+
+const char* kvsel_status_string(kvsel_status s) {
+  switch (s) {
+    case KVSEL_OK: return "ok";
+    case KVSEL_ERR_INVALID_ARG: return "invalid argument";
+    case KVSEL_ERR_UNSUPPORTED: return "unsupported (beyond a documented limit)";
+    case KVSEL_ERR_NONFINITE: return "non-finite window logit or score";
+    case KVSEL_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case KVSEL_ERR_CUDA: return "CUDA runtime error";
+    case KVSEL_ERR_BAD_INDEX: return "gather index out of range";
+    default: return "unknown status";
+  }
+}
+
+int64_t kvsel_out_tokens(const kvsel_shape* shape, int32_t C) {
+  if (C < 1) return -1;
+  Plan p;
+  if (plan_shape(shape, C, &p) != KVSEL_OK) return -1;
+  return p.T_out;
+}
+
+int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C) {
+  Plan p;
+  if (C < 0 || plan_shape(shape, C, &p) != KVSEL_OK) return -1;
+  if (check_window(p, W) != KVSEL_OK) return -1;
+  if (C > 0 && check_budget(W, C) != KVSEL_OK) return -1;
+  DevState* d = nullptr;
+  if (device_state(&d) != KVSEL_OK) return -1;
+  ScorePlan sp;
+  // alignment is unknown here: assume 256-byte aligned tensors
+  static const char probe[32] = {0};
+  const void* aligned = reinterpret_cast<const void*>(
+      (reinterpret_cast<uintptr_t>(probe) + 255) & ~uintptr_t(255));
+  if (plan_score(p, W, C, aligned, aligned, d, &sp) != KVSEL_OK) return -1;
+  return sp.tc ? 1 : 0;
+}
+
+kvsel_status kvsel_window_logits(const kvsel_shape* shape, const void* q_win, const void* K,
+                                 int32_t W, float* logits, void* stream) {
+  Plan p;
+  kvsel_status st;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if (p.T == 0) return KVSEL_OK;
+  if (!q_win || !K || !logits) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  ScorePlan sp;
+  if ((st = plan_score(p, W, 0, q_win, K, d, &sp))) return st;
+  char* ws;
+  if ((st = workspace(d, score_ws_bytes(p, sp), &ws))) return st;
+  Carve cv;
+  return run_score(p, sp, d, q_win, K, W, nullptr, logits, ws, cv,
+                   static_cast<cudaStream_t>(stream));
+}
+
+kvsel_status kvsel_score(const kvsel_shape* shape, const void* q_win, const void* K, int32_t W,
+                         int32_t pool_kind, int32_t pool_k, float* votes, float* pooled,
+                         void* stream) {
+  Plan p;
+  kvsel_status st;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_pool(pool_kind, pool_k))) return st;
+  if (p.T == 0) return KVSEL_OK;
+  if (!q_win || !K || !pooled) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  ScorePlan sp;
+  if ((st = plan_score(p, W, 0, q_win, K, d, &sp))) return st;
+  const size_t votes_bytes = votes ? 0 : (size_t)p.layers * p.H * p.T * sizeof(float);
+  char* ws;
+  if ((st = workspace(d, score_ws_bytes(p, sp) + votes_bytes +
+                             p.all.size() * sizeof(SeqDesc) + 1024, &ws)))
+    return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  float* v = votes;
+  if (!v) v = reinterpret_cast<float*>(ws + cv.take(votes_bytes));
+  if ((st = run_score(p, sp, d, q_win, K, W, v, nullptr, ws, cv, s))) return st;
+  PoolArgs pa{};
+  pa.votes = v;
+  pa.pooled = pooled;
+  pa.layers = p.layers;
+  pa.H = p.H;
+  pa.W = W;
+  pa.pool_kind = pool_kind;
+  pa.pool_k = pool_k;
+  pa.T = p.T;
+  pa.n_seqs = p.S;
+  pa.seqs = all_dev;
+  pa.stream = s;
+  return cuda_fail(launch_pool(pa), "pooling launch");
+}
+
+kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t W, int32_t C,
+                          int32_t* out_idx, void* stream) {
+  Plan p;
+  kvsel_status st;
+  if (C < 1) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_budget(W, C))) return st;
+  if (p.T_out == 0) return KVSEL_OK;
+  if (!pooled || !out_idx) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  char* ws;
+  if ((st = workspace(d, p.all.size() * sizeof(SeqDesc) + 1024, &ws))) return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  SelectArgs sa{};
+  sa.scores = pooled;
+  sa.pooled_ws = nullptr;
+  sa.pool_inline = 0;
+  sa.layers = p.layers;
+  sa.H = p.H;
+  sa.W = W;
+  sa.C = C;
+  sa.T = p.T;
+  sa.T_out = p.T_out;
+  sa.n_seqs = p.S;
+  sa.seqs = all_dev;
+  sa.out_idx = out_idx;
+  sa.status = d->status;
+  sa.sm_count = d->sm_count;
+  sa.stream = s;
+  return cuda_fail(launch_select(sa), "selection launch");
+}
+
+kvsel_status kvsel_compact(const kvsel_shape* shape, const void* K, const void* V,
+                           const int32_t* out_idx, int32_t C, void* out_K, void* out_V,
+                           void* stream) {
+  Plan p;
+  kvsel_status st;
+  if (C < 1) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if (p.T_out == 0) return KVSEL_OK;
+  if (!K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  char* ws;
+  if ((st = workspace(d, p.all.size() * sizeof(SeqDesc) + 1024, &ws))) return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  CompactArgs ca{};
+  ca.k = K;
+  ca.v = V;
+  ca.idx = out_idx;
+  ca.out_k = out_K;
+  ca.out_v = out_V;
+  ca.layers = p.layers;
+  ca.H = p.H;
+  ca.S = p.S;
+  ca.C = C;
+  ca.T = p.T;
+  ca.T_out = p.T_out;
+  ca.row_bytes = (int64_t)p.D * p.elem_bytes;
+  ca.seqs = all_dev;
+  int64_t mr = 0;
+  for (const SeqDesc& q : p.all) {
+    const int64_t n = (int64_t)(q.len < C ? q.len : C) * p.H;
+    if (n > mr) mr = n;
+  }
+  ca.max_rows = mr;
+  if ((double)mr * (double)(ca.row_bytes / 2) > 4.0e9) return KVSEL_ERR_UNSUPPORTED;
+  ca.status = d->status;
+  ca.sm_count = d->sm_count;
+  ca.stream = s;
+  return cuda_fail(launch_compact(ca), "gather launch");
+}
+
+kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const void* K,
+                          const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                          int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                          void* stream) {
+  Plan p;
+  kvsel_status st;
+  if (C < 1) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_budget(W, C))) return st;
+  if ((st = check_pool(pool_kind, pool_k))) return st;
+  if (p.T_out == 0) return KVSEL_OK;
+  if (!q_win || !K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  ScorePlan sp;
+  if ((st = plan_score(p, W, C, q_win, K, d, &sp))) return st;
+  const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
+  char* ws;
+  if ((st = workspace(d, score_ws_bytes(p, sp) + 2 * plane_bytes + 2 * 256 +
+                             p.all.size() * sizeof(SeqDesc) + 1024, &ws)))
+    return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  float* votes = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
+  float* pooled = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
+  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s))) return st;
+  SelectArgs sa{};
+  sa.scores = votes;
+  sa.pooled_ws = pooled;
+  sa.pool_inline = 1;
+  sa.pool_kind = pool_kind;
+  sa.pool_k = pool_k;
+  sa.layers = p.layers;
+  sa.H = p.H;
+  sa.W = W;
+  sa.C = C;
+  sa.T = p.T;
+  sa.T_out = p.T_out;
+  sa.n_seqs = p.S;
+  sa.seqs = all_dev;
+  sa.out_idx = out_idx;
+  sa.status = d->status;
+  sa.sm_count = d->sm_count;
+  sa.stream = s;
+  if ((st = cuda_fail(launch_select(sa), "selection launch"))) return st;
+  CompactArgs ca{};
+  ca.k = K;
+  ca.v = V;
+  ca.idx = out_idx;
+  ca.out_k = out_K;
+  ca.out_v = out_V;
+  ca.layers = p.layers;
+  ca.H = p.H;
+  ca.S = p.S;
+  ca.C = C;
+  ca.T = p.T;
+  ca.T_out = p.T_out;
+  ca.row_bytes = (int64_t)p.D * p.elem_bytes;
+  ca.seqs = all_dev;
+  int64_t mr = 0;
+  for (const SeqDesc& q : p.all) {
+    const int64_t n = (int64_t)(q.len < C ? q.len : C) * p.H;
+    if (n > mr) mr = n;
+  }
+  ca.max_rows = mr;
+  ca.status = d->status;
+  ca.sm_count = d->sm_count;
+  ca.stream = s;
+  return cuda_fail(launch_compact(ca), "gather launch");
+}
+
+kvsel_status kvsel_device_status(void* stream) {
+  DevState* d;
+  kvsel_status st;
+  if ((st = device_state(&d))) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "cudaMemcpy(status)");
+  if ((e = cudaMemset(d->status, 0, sizeof(int)))) return cuda_fail(e, "cudaMemset(status)");
+  return v;
+}
+
+kvsel_status kvsel_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000) return KVSEL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_limit_ns = ns;
+  return KVSEL_OK;
+}
+
+kvsel_status kvsel_debug_inject(int32_t what) {
+  if (what != 0 && what != 1) return KVSEL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_inject = what;
+  return KVSEL_OK;
+}
+
+void kvsel_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (int i = 0; i < kMaxDevices; ++i) {
+    if (g_dev[i].ws) {
+      cudaSetDevice(i);
+      cudaDeviceSynchronize();
+      cudaFree(g_dev[i].ws);
+      g_dev[i].ws = nullptr;
+      g_dev[i].ws_bytes = 0;
+    }
+  }
+  cudaSetDevice(cur);
+}
+
+}  // extern "C"

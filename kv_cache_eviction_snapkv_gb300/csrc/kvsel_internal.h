@@ -1,0 +1,110 @@
+// Host-side plumbing shared by the libkvsel translation units: the per-call
+// descriptors handed to each kernel's launch wrapper. No device code here.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvsel.h"
+
+namespace kvsel {
+
+// One sequence as the kernels see it (copied to device memory per call).
+struct SeqDesc {
+  int64_t tok_off;    // first token of the sequence within a layer
+  int32_t len;        // L_b
+  int32_t out_off;    // first output row within a layer: sum_{b'<b} min(L_b', C)
+  int32_t n_chunks;   // scoring work items per head (0: not scored)
+  int32_t item_base;  // first scoring work item of this sequence within a layer
+  int32_t inst_base;  // instance id of (this sequence, head 0) within a layer
+  int32_t index;      // position of the sequence in the call (row block of q_win)
+};
+static_assert(sizeof(SeqDesc) == 32, "SeqDesc layout");
+
+// Scoring: window logits -> causal softmax row statistics -> votes.
+// Work item = (layer, scored sequence, head, chunk of chunk_tokens tokens);
+// instance = (layer, scored sequence, head).
+struct ScoreArgs {
+  const void* q;           // q_win
+  const void* k;           // K
+  int layers, H, D, dtype, W;
+  int64_t T;               // tokens per layer
+  int64_t q_rows;          // rows of q_win per layer (num_seqs * W)
+  int n_scored;            // number of scored sequences
+  const SeqDesc* seqs;     // device: the scored sequences, in order
+  int items_per_layer, inst_per_layer;
+  int chunk_tokens;
+  int wpad;                // row stride of part / final_stats (>= W)
+  float scale_log2;        // log2(e) / sqrt(D): logits in base-2 units
+  float scale;             // 1 / sqrt(D): logits as the page defines them
+  float* part;             // [items][Wp][2] chunk (max, sum) in base-2 units
+  int* counters;           // [instances] chunks that published their stats
+  int* flags;              // [instances] 1 once the merged stats are written
+  float* final_stats;      // [instances][Wp] max + log2(sum) per window row
+  float* votes;            // [layers][H][T]
+  float* logits;           // [layers][H][W][T] (logits mode only)
+  int* status;             // device status word
+  unsigned long long wait_limit_ns;
+  int inject;              // test hook (see kvsel_debug_inject)
+  int sm_count;
+  cudaStream_t stream;
+};
+
+struct PoolArgs {
+  const float* votes;      // [layers][H][T]
+  float* pooled;           // [layers][H][T]
+  int layers, H, W, pool_kind, pool_k;
+  int64_t T;
+  int n_seqs;
+  const SeqDesc* seqs;     // every sequence (pooled is computed where L >= W)
+  cudaStream_t stream;
+};
+
+struct SelectArgs {
+  const float* scores;     // pooled, or votes when pool_inline
+  float* pooled_ws;        // pool_inline: pooled scores written here
+  int pool_inline, pool_kind, pool_k;
+  int layers, H, W, C;
+  int64_t T, T_out;
+  int n_seqs;
+  const SeqDesc* seqs;     // every sequence
+  int32_t* out_idx;
+  int* status;
+  int sm_count;
+  cudaStream_t stream;
+};
+
+struct CompactArgs {
+  const void* k;
+  const void* v;
+  const int32_t* idx;
+  void* out_k;
+  void* out_v;
+  int layers, H, S, C;
+  int64_t T, T_out;
+  int64_t row_bytes;
+  const SeqDesc* seqs;     // every sequence
+  int64_t max_rows;        // max over sequences of min(L, C) * H
+  int* status;
+  int sm_count;
+  cudaStream_t stream;
+};
+
+constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
+constexpr int kGenericChunk = 256;   // tokens per CUDA-core scoring block
+constexpr int kGenericMaxQ = 16384;  // W * D floats staged in shared memory
+
+// Launch wrappers (each defined beside its kernels).
+cudaError_t launch_generic_score(const ScoreArgs& a, bool logits_mode);
+cudaError_t launch_pool(const PoolArgs& a);
+cudaError_t launch_select(const SelectArgs& a);
+cudaError_t launch_compact(const CompactArgs& a);
+
+// Tensor-core path.
+int tc_window_pad(int W);                       // padded MMA N for W, 0 if unsupported
+int tc_chunk_tokens(int W);                     // tokens per CTA work item
+bool tc_eligible(int dtype, int D, int W, const void* q, const void* k);
+cudaError_t launch_tc_score(const ScoreArgs& a, bool logits_mode, int grid);
+int tc_max_grid(int sm_count);                  // co-resident CTAs (one per SM)
+
+}  // namespace kvsel
