@@ -172,6 +172,16 @@ kvsel_status kvsel_set_wait_limit_ns(uint64_t ns);
  * KVSEL_ERR_TIMEOUT. what = 0 clears it. */
 kvsel_status kvsel_debug_inject(int32_t what);
 
+/* Stage timing of kvsel_snapkv with CUDA events recorded on the caller's
+ * stream around each stage: [0] scoring kernel(s), [1] selection kernel,
+ * [2] gather kernel. kvsel_profile_begin(n) arms it for the next n calls on
+ * the current device (n in 1..100000; creates the events); each call records
+ * its events without synchronising. kvsel_profile_end() synchronises, writes
+ * the summed milliseconds per stage to stage_ms[0..2] and the number of
+ * recorded calls to *calls, and disarms. */
+kvsel_status kvsel_profile_begin(int32_t max_calls);
+kvsel_status kvsel_profile_end(double* stage_ms, int32_t* calls);
+
 /* Frees the internal workspace of every device this process used. Calls
  * still running on the GPU must have finished (the call synchronises each
  * device first). */

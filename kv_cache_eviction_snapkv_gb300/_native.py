@@ -36,6 +36,8 @@ SIGNATURES = {
     "kvsel_device_status": (c_i32, [c_vp]),
     "kvsel_set_wait_limit_ns": (c_i32, [c_u64]),
     "kvsel_debug_inject": (c_i32, [c_i32]),
+    "kvsel_profile_begin": (c_i32, [c_i32]),
+    "kvsel_profile_end": (c_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i32)]),
     "kvsel_release": (None, []),
 }
 

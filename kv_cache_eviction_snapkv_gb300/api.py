@@ -224,5 +224,17 @@ def kvsel_debug_inject(what: int) -> None:
     _check(_native.lib().kvsel_debug_inject(int(what)), "kvsel_debug_inject")
 
 
+def kvsel_profile_begin(max_calls: int) -> None:
+    _check(_native.lib().kvsel_profile_begin(int(max_calls)), "kvsel_profile_begin")
+
+
+def kvsel_profile_end():
+    """(summed ms per stage [score, select, gather], number of recorded calls)."""
+    ms = (ctypes.c_double * 3)()
+    calls = ctypes.c_int32(0)
+    _check(_native.lib().kvsel_profile_end(ms, ctypes.byref(calls)), "kvsel_profile_end")
+    return [ms[0], ms[1], ms[2]], calls.value
+
+
 def kvsel_release() -> None:
     _native.lib().kvsel_release()

@@ -37,6 +37,25 @@ DevState g_dev[kMaxDevices];
 unsigned long long g_wait_limit_ns = 2000000000ull;
 int g_inject = 0;
 
+// Stage-timing events for kvsel_snapkv (see kvsel_profile_begin).
+struct Profile {
+  bool armed = false;
+  int device = -1;
+  int capacity = 0, used = 0;
+  std::vector<cudaEvent_t> ev;  // 4 per call
+};
+Profile g_prof;
+
+// Event slot for the next fused call, or nullptr when profiling is off.
+cudaEvent_t* profile_slot() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_prof.armed || g_prof.used >= g_prof.capacity) return nullptr;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != g_prof.device) return nullptr;
+  return &g_prof.ev[4 * (size_t)g_prof.used++];
+}
+
 kvsel_status cuda_fail(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return KVSEL_OK;
   std::fprintf(stderr, "libkvsel: %s failed: %s\n", what, cudaGetErrorString(e));
@@ -202,8 +221,9 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
   };
   if (tc_ok) {
     build(tc_chunk_tokens(W));
-    // every chunk of one instance must be resident at once (one CTA per SM)
-    if (sp->max_chunks <= tc_max_grid(d->sm_count)) {
+    // the waits between the chunks of one instance end only if every chunk
+    // can be in flight at once (chunks <= CTAs x TMEM buffers per CTA)
+    if (sp->max_chunks <= tc_max_chunks(W, d->sm_count)) {
       sp->tc = true;
       sp->chunk = tc_chunk_tokens(W);
       sp->wpad = tc_window_pad(W);
@@ -221,7 +241,7 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
 // Uploads the sequence tables and runs the scoring kernels (votes or logits).
 kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const void* q,
                        const void* k, int W, float* votes, float* logits, char* ws,
-                       Carve& cv, cudaStream_t stream) {
+                       Carve& cv, cudaStream_t stream, cudaEvent_t* ev = nullptr) {
   const int64_t items = (int64_t)p.layers * sp.items_per_layer;
   const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
   if (items == 0) return KVSEL_OK;
@@ -268,14 +288,19 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
     if (sp.tc && logits == nullptr) g_inject = 0;  // one-shot
   }
   if (sp.tc) {
-    if ((e = cudaMemsetAsync(a.counters, 0, (size_t)insts * 2 * sizeof(int), stream)))
-      return cuda_fail(e, "cudaMemsetAsync(counters)");
+    // the tensor-core kernel's exchange slots start out as all-ones (empty)
+    if ((e = cudaMemsetAsync(a.part, 0xFF, (size_t)items * sp.wpad * 2 * sizeof(float), stream)))
+      return cuda_fail(e, "cudaMemsetAsync(exchange slots)");
     int grid = tc_max_grid(d->sm_count);
     if (items < grid) grid = (int)items;
+    if (ev) cudaEventRecord(ev[0], stream);
     e = launch_tc_score(a, logits != nullptr, grid);
+    if (ev) cudaEventRecord(ev[1], stream);
     return cuda_fail(e, "tensor-core scoring launch");
   }
+  if (ev) cudaEventRecord(ev[0], stream);
   e = launch_generic_score(a, logits != nullptr);
+  if (ev) cudaEventRecord(ev[1], stream);
   return cuda_fail(e, "CUDA-core scoring launch");
 }
 
@@ -510,7 +535,8 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
   float* votes = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
   float* pooled = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
-  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s))) return st;
+  cudaEvent_t* ev = profile_slot();
+  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s, ev))) return st;
   SelectArgs sa{};
   sa.scores = votes;
   sa.pooled_ws = pooled;
@@ -530,6 +556,7 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   sa.sm_count = d->sm_count;
   sa.stream = s;
   if ((st = cuda_fail(launch_select(sa), "selection launch"))) return st;
+  if (ev) cudaEventRecord(ev[2], s);
   CompactArgs ca{};
   ca.k = K;
   ca.v = V;
@@ -553,7 +580,9 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   ca.status = d->status;
   ca.sm_count = d->sm_count;
   ca.stream = s;
-  return cuda_fail(launch_compact(ca), "gather launch");
+  if ((st = cuda_fail(launch_compact(ca), "gather launch"))) return st;
+  if (ev) cudaEventRecord(ev[3], s);
+  return KVSEL_OK;
 }
 
 kvsel_status kvsel_device_status(void* stream) {
@@ -581,6 +610,42 @@ kvsel_status kvsel_debug_inject(int32_t what) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_inject = what;
   return KVSEL_OK;
+}
+
+kvsel_status kvsel_profile_begin(int32_t max_calls) {
+  if (max_calls < 1 || max_calls > 100000) return KVSEL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof = Profile();
+  cudaError_t e = cudaGetDevice(&g_prof.device);
+  if (e) return cuda_fail(e, "cudaGetDevice");
+  g_prof.ev.resize(4 * (size_t)max_calls);
+  for (auto& ev : g_prof.ev)
+    if ((e = cudaEventCreate(&ev))) return cuda_fail(e, "cudaEventCreate");
+  g_prof.capacity = max_calls;
+  g_prof.armed = true;
+  return KVSEL_OK;
+}
+
+kvsel_status kvsel_profile_end(double* stage_ms, int32_t* calls) {
+  if (!stage_ms || !calls) return KVSEL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  stage_ms[0] = stage_ms[1] = stage_ms[2] = 0.0;
+  *calls = g_prof.used;
+  kvsel_status st = KVSEL_OK;
+  for (int c = 0; c < g_prof.used && st == KVSEL_OK; ++c) {
+    cudaEvent_t* ev = &g_prof.ev[4 * (size_t)c];
+    cudaError_t e = cudaEventSynchronize(ev[3]);
+    for (int i = 0; i < 3 && !e; ++i) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, ev[i], ev[i + 1]);
+      stage_ms[i] += ms;
+    }
+    if (e) st = cuda_fail(e, "cudaEventElapsedTime");
+  }
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof = Profile();
+  return st;
 }
 
 void kvsel_release(void) {

@@ -106,5 +106,6 @@ int tc_chunk_tokens(int W);                     // tokens per CTA work item
 bool tc_eligible(int dtype, int D, int W, const void* q, const void* k);
 cudaError_t launch_tc_score(const ScoreArgs& a, bool logits_mode, int grid);
 int tc_max_grid(int sm_count);                  // co-resident CTAs (one per SM)
+int tc_max_chunks(int W, int sm_count);         // most chunks one instance may have
 
 }  // namespace kvsel

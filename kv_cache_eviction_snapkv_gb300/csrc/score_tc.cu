@@ -45,9 +45,7 @@
 namespace kvsel {
 namespace {
 
-constexpr int kThreads = 320;         // 10 warps
-constexpr int kEpiWarps = 8;          // warps 2..9
-constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kGroupThreads = 256;   // one epilogue group: 8 warps, 2 per TMEM lane quarter
 constexpr int kTileM = 128;           // tokens per MMA tile
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 512;
@@ -61,19 +59,36 @@ struct TcParams {
   int n_items;
 };
 
+// Epilogue groups for a padded window NW: two groups ping-pong over the two
+// halves of TMEM when their per-thread state fits the register budget of
+// 64 + 2 * 256 threads, else one group owns all of TMEM.
+__host__ __device__ constexpr int groups_for(int nw) { return nw <= 32 ? 2 : 1; }
+__host__ __device__ constexpr int threads_for(int nw) { return 64 + groups_for(nw) * kGroupThreads; }
+__host__ __device__ constexpr int tiles_per_item(int nw) { return kTmemCols / groups_for(nw) / nw; }
+// Registers per thread such that the CTA fits the register file of each SM
+// sub-partition (16K registers; warps are spread round-robin over the four,
+// so the busiest one holds ceil(warps / 4) warps): 18 warps -> 96, 10 -> 168.
+__host__ __device__ constexpr int regs_for(int nw) {
+  return (16384 / (((threads_for(nw) / 32) + 3) / 4 * 32)) / 8 * 8;
+}
+
+struct GroupState {
+  unsigned long long tile_ready[32];    // MMA -> epilogue, one per TMEM tile
+  unsigned long long tmem_empty;        // epilogue -> MMA, the group's TMEM half is free
+  int snap;                             // abort flag as seen by one thread of the group
+  int timed_out;
+  float wm[4][64], wz[4][64];           // per lane quarter row statistics
+  float fin[64];                        // M_r + log2 Z_r (+inf for padded rows)
+  float2 cst[64];                       // this chunk's (reference, sum) per row
+};
+
 struct Misc {
   unsigned long long full[kMaxStages], empty[kMaxStages];
   unsigned long long qfull[2], qempty[2];
-  unsigned long long tile_ready[32];
-  unsigned long long tmem_empty, mma_done;
+  unsigned long long mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
-  int timed_out;
-  int snap;                             // abort flag as seen by one epilogue thread
-  float sref[kEpiWarps][64];           // per-warp broadcast of running row maxima
-  float wm[kEpiWarps][64], wz[kEpiWarps][64];
-  float fin[64];                        // M_r + log2 Z_r (+inf for padded rows)
+  GroupState g[2];
 };
 
 // ---------------------------------------------------------------------------
@@ -111,10 +126,9 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with `parity`; gives up when the limit passes or
 // (if `abort_flag` is non-null) when another role has given up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                       unsigned long long limit_ns,
-                                       const volatile int* abort_flag) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            unsigned long long limit_ns,
+                                            const volatile int* abort_flag) {
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(bar, parity)) return true;
@@ -123,6 +137,31 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
       if (global_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns,
+                                          const volatile int* abort_flag) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, limit_ns, abort_flag);
+}
+
+// Row statistics slots of the cross-chunk exchange: one 8-byte (reference,
+// sum) pair per (work item, row), pre-filled with an all-ones pattern (a NaN
+// reference, which a published pair never has). A relaxed 8-byte store is
+// single-copy atomic, so a reader that sees a value other than the pattern
+// sees the whole pair.
+constexpr unsigned long long kEmptySlot = ~0ull;
+
+__device__ __forceinline__ void slot_publish(unsigned long long* slot, float m, float z) {
+  const unsigned long long v =
+      ((unsigned long long)__float_as_uint(z) << 32) | __float_as_uint(m);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(slot), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long slot_read(const unsigned long long* slot) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(slot) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -218,6 +257,14 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// After tcgen05.wait::ld: ties each loaded value to an empty volatile asm that
+// follows the wait, so no use of the value can be scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void after_wait(float (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
+
 template <int NW>
 __device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&v)[NW]) {
   if constexpr (NW == 16) {
@@ -227,49 +274,89 @@ __device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&v)[NW]) {
     for (int c = 0; c < NW; c += 32) tmem_ld32(taddr + c, v + c);
   }
   tmem_wait_ld();
+  after_wait(v);
 }
 
-__device__ __forceinline__ void epi_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// Transposed butterfly reduction over the 32 lanes of a warp: each lane starts
-// with NW per-row values for its own token and ends with the reduction over
-// all 32 tokens of RPL = max(1, NW/32) rows: rows 2*lane, 2*lane+1 (NW = 64),
-// row lane (NW = 32) or row lane/2 (NW = 16).
-// ---------------------------------------------------------------------------
-
-template <int NW>
-__device__ __forceinline__ int row_of(int lane, int i) {
-  if constexpr (NW == 64) return 2 * lane + i;
-  else if constexpr (NW == 32) return lane;
-  else return lane >> 1;
-}
-
-template <int NW, bool MAX>
-__device__ __forceinline__ void reduce_rows(float (&v)[NW], int lane) {
-  int count = NW;
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : KVSEL_R8(0)
+               : "r"(taddr));
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    if (count >= 2) {
-      const int half = count >> 1;
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < NW / 2; ++i) {
-        if (i < half) {
-          const float send = upper ? v[i] : v[i + half];
-          const float keep = upper ? v[i + half] : v[i];
-          const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-          v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
-        }
-      }
-      count = half;
-    } else {
-      const float recv = __shfl_xor_sync(0xffffffffu, v[0], off);
-      v[0] = MAX ? fmaxf(v[0], recv) : v[0] + recv;
-    }
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// One column, no wait (tcgen05.wait::ld and after_wait must follow).
+__device__ __forceinline__ float tmem_ld1_nowait(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  float v[1] = {tmem_ld1_nowait(taddr)};
+  tmem_wait_ld();
+  after_wait(v);
+  return v[0];
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+               "r"(__float_as_uint(v))
+               : "memory");
+}
+
+#define KVSEL_W8(i) "r"(__float_as_uint(v[i])), "r"(__float_as_uint(v[i + 1])), \
+                    "r"(__float_as_uint(v[i + 2])), "r"(__float_as_uint(v[i + 3])), \
+                    "r"(__float_as_uint(v[i + 4])), "r"(__float_as_uint(v[i + 5])), \
+                    "r"(__float_as_uint(v[i + 6])), "r"(__float_as_uint(v[i + 7]))
+
+// Stores N consecutive TMEM columns of this thread's lane (N = 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)[N]) {
+  if constexpr (N == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), KVSEL_W8(0) : "memory");
+  } else if constexpr (N == 16) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), KVSEL_W8(0), KVSEL_W8(8) : "memory");
+  } else {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 ::"r"(taddr), KVSEL_W8(0), KVSEL_W8(8), KVSEL_W8(16), KVSEL_W8(24)
+                 : "memory");
   }
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// N consecutive TMEM columns of this thread's lane (N = 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_load_cols_nowait(uint32_t taddr, float* v) {
+  if constexpr (N == 8) tmem_ld8(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[N]) {
+  tmem_load_cols_nowait<N>(taddr, v);
+  tmem_wait_ld();
+  after_wait(v);
+}
+
+// All threads of epilogue group g (named barriers 1, 2).
+__device__ __forceinline__ void epi_bar(int g) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads) : "memory");
+}
+
+// The two warps of group g on TMEM lane quarter q (named barriers 3..10).
+__device__ __forceinline__ void pair_bar(int g, int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(3 + 4 * g + q) : "memory");
 }
 
 // (m1, z1) merged with (m2, z2), sums relative to the merged max.
@@ -282,16 +369,49 @@ __device__ __forceinline__ void merge_stats(float& m1, float& z1, float m2, floa
   z1 = a + b;
 }
 
+// Transposed butterfly over the 32 lanes for N (reference, sum) pairs per
+// lane: afterwards lane l holds the merged pair of row l / (32 / N) (N <= 32).
+template <int N>
+__device__ __forceinline__ void reduce_stats(float (&m)[N], float (&z)[N], int lane) {
+  int count = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (count >= 2) {
+      const int half = count >> 1;
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float sm = upper ? m[i] : m[i + half], sz = upper ? z[i] : z[i + half];
+          float km = upper ? m[i + half] : m[i], kz = upper ? z[i + half] : z[i];
+          const float rm = __shfl_xor_sync(0xffffffffu, sm, off);
+          const float rz = __shfl_xor_sync(0xffffffffu, sz, off);
+          merge_stats(km, kz, rm, rz);
+          m[i] = km;
+          z[i] = kz;
+        }
+      }
+      count = half;
+    } else {
+      const float rm = __shfl_xor_sync(0xffffffffu, m[0], off);
+      const float rz = __shfl_xor_sync(0xffffffffu, z[0], off);
+      merge_stats(m[0], z[0], rm, rz);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
 template <int NW, int KD, bool LOGITS>
-__global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_constant__ TcParams P) {
+__global__ void __maxnreg__(regs_for(NW)) tc_score_kernel(const __grid_constant__ TcParams P) {
   constexpr int kHalves = KD / 64;
   constexpr int kStageBytes = kTileM * KD * 2;
   constexpr int kQBytes = NW * KD * 2;
-  constexpr int kRPL = NW >= 32 ? NW / 32 : 1;
+  constexpr int kG = groups_for(NW);
+  constexpr int kBufCols = kTmemCols / kG;     // TMEM columns of one group
+  constexpr int kTiles = kBufCols / NW;        // tiles per work item
   constexpr uint32_t kIdesc = instr_desc(NW, kTileM);
   const ScoreArgs& a = P.a;
   const int stages = P.stages;
@@ -317,8 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
       mbar_init(smem_u32(&ms->qfull[b]), 1);
       mbar_init(smem_u32(&ms->qempty[b]), 1);
     }
-    for (int t = 0; t < 32; ++t) mbar_init(smem_u32(&ms->tile_ready[t]), 1);
-    mbar_init(smem_u32(&ms->tmem_empty), kEpiWarps);
+    for (int g = 0; g < kG; ++g) {
+      for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&ms->g[g].tile_ready[t]), 1);
+      mbar_init(smem_u32(&ms->g[g].tmem_empty), 8);
+    }
     mbar_init(smem_u32(&ms->mma_done), 1);
     ms->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -349,8 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
       const uint64_t pol_q = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0;  // bit s: stage s armed at least once
-      uint32_t last_par = 0;
+      uint32_t armed = 0, last_par = 0;
       bool ok = true;
       for (int it = 0, item = blockIdx.x; ok && item < P.n_items; ++it, item += gridDim.x) {
         const ItemPos ip = decode_item(a, item);
@@ -409,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
         const int ntok = min(a.chunk_tokens, sd.len - tok0);
         const int ntiles = (ntok + kTileM - 1) / kTileM;
         const int qb = it & 1;
-        if (!mbar_wait(smem_u32(&ms->tmem_empty), (it & 1) ^ 1, limit, abort_flag) ||
+        const int g = it % kG;
+        GroupState& gs = ms->g[g];
+        if (!mbar_wait(smem_u32(&gs.tmem_empty), ((it / kG) & 1) ^ 1, limit, abort_flag) ||
             !mbar_wait(smem_u32(&ms->qfull[qb]), (it >> 1) & 1, limit, abort_flag)) {
           ok = false;
           break;
@@ -421,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(t * NW);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(g * kBufCols + t * NW);
 #pragma unroll
           for (int kk = 0; kk < KD / 16; ++kk) {
             const uint32_t a_addr =
@@ -431,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
           }
           issued = true;
           tc_commit(smem_u32(&ms->empty[stage]));
-          tc_commit(smem_u32(&ms->tile_ready[t]));
+          tc_commit(smem_u32(&gs.tile_ready[t]));
           if (++stage == stages) {
             stage = 0;
             phase ^= 1;
@@ -447,13 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 2;             // 0..7
-    const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31
-    const int sub = e >> 2;             // tiles t = sub, sub + 2, ...
-    const int et = threadIdx.x - 64;    // 0..255
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * quarter) << 16);
-    uint32_t tph = 0;                   // per tile barrier: parity of the next phase
-    for (int it = 0, item = blockIdx.x; item < P.n_items; ++it, item += gridDim.x) {
+    const int g = (warp - 2) >> 3;          // group: the CTA's items it = g, g + kG, ...
+    GroupState& gs = ms->g[g];
+    const int e = (warp - 2) & 7;
+    const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+    const int sub = e >> 2;                 // row half (votes) / tile parity (logits)
+    const int et = threadIdx.x - 64 - g * kGroupThreads;   // 0..255 within the group
+    const uint32_t lane_addr =
+        tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(g * kBufCols);
+    uint32_t tph = 0;                       // per tile barrier: parity of the next phase
+    for (int it = g, item = blockIdx.x + g * gridDim.x; item < P.n_items;
+         it += kG, item += kG * gridDim.x) {
       const ItemPos ip = decode_item(a, item);
       const SeqDesc sd = a.seqs[ip.s];
       const int tok0 = ip.c * a.chunk_tokens;
@@ -465,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
 
       if constexpr (LOGITS) {
         for (int t = sub; t < ntiles; t += 2) {
-          if (ok && !mbar_wait(smem_u32(&ms->tile_ready[t]), (tph >> t) & 1, limit, abort_flag))
-            ok = false;
+          if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&gs.tile_ready[t]), (tph >> t) & 1,
+                                                   limit, abort_flag));
           tph ^= 1u << t;
           if (!ok) continue;
           tc_fence_after();
@@ -485,104 +613,158 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
           record_status(a.status, KVSEL_ERR_TIMEOUT);
         }
       } else {
-        // ---- pass A: running (max, sum) per row over this warp's tokens
-        float mrun[kRPL], zrun[kRPL];
+        // ---- pass A: per-row softmax statistics of this warp's tokens. The two
+        // warps of a lane quarter split the rows (half `sub` = rows sub*NH ..
+        // sub*NH + NH - 1) and see every tile. Each thread keeps, per row, a
+        // reference value and the sum of 2^(x - reference) over its own
+        // tokens; the reference moves only when a logit exceeds it by more
+        // than 32 (so no term exceeds 2^32), which after the first visible
+        // token is rare. The exponentials replace the logits in TMEM.
+        constexpr int NH = NW / 2;
+        float mref[NH], zsum[NH];
 #pragma unroll
-        for (int i = 0; i < kRPL; ++i) {
-          mrun[i] = -INFINITY;
-          zrun[i] = 0.f;
+        for (int i = 0; i < NH; ++i) {
+          mref[i] = -INFINITY;
+          zsum[i] = 0.f;
         }
         bool bad = false;
-        for (int t = sub; t < ntiles; t += 2) {
-          if (ok && !mbar_wait(smem_u32(&ms->tile_ready[t]), (tph >> t) & 1, limit, abort_flag))
-            ok = false;
+        const int row0 = sub * NH;
+        for (int t = 0; t < ntiles; ++t) {
+          // warp-uniform: the TMEM loads and stores below are .sync.aligned
+          if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&gs.tile_ready[t]), (tph >> t) & 1,
+                                                   limit, abort_flag));
           tph ^= 1u << t;
           if (!ok) continue;
           tc_fence_after();
-          float x[NW], y[NW];
-          tmem_load_row<NW>(lane_addr + (uint32_t)(t * NW), x);
+          float x[NH];
+          tmem_load_cols<NH>(lane_addr + (uint32_t)(t * NW + row0), x);
           const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-          const bool tv = tok < sd.len;
+          // rows visible to this token: row0 + i < W, and tok <= P + row0 + i
+          const int lo = max(0, tok - prefix - row0);
+          const int hi = tok < sd.len ? min(NH, W - row0) : 0;
+          bool need = false, fixany = false;
 #pragma unroll
-          for (int r = 0; r < NW; ++r) {
-            x[r] *= a.scale_log2;
-            const bool in = tv && r < W;
-            if (in && !finite_f(x[r])) bad = true;
-            y[r] = (in && tok <= prefix + r) ? x[r] : -INFINITY;
+          for (int i = 0; i < NH; ++i) {
+            x[i] *= a.scale_log2;
+            const bool in = i < hi;
+            if (in && !finite_f(x[i])) bad = true;
+            const bool up = in && i >= lo && x[i] > mref[i] + 32.f;
+            need |= up;
+            fixany |= up && mref[i] != -INFINITY;
           }
-          reduce_rows<NW, true>(y, lane);
+          if (__any_sync(0xffffffffu, fixany)) {
+            // A logit more than 2^32 above a finite reference (rare): rescale
+            // the exponentials already stored for that row before moving it.
 #pragma unroll
-          for (int i = 0; i < kRPL; ++i) {
-            const float mn = fmaxf(mrun[i], y[i]);
-            if (mn > mrun[i]) {
-              zrun[i] = mrun[i] == -INFINITY ? 0.f : zrun[i] * ex2(mrun[i] - mn);
-              mrun[i] = mn;
+            for (int i = 0; i < NH; ++i) {
+              const bool fix = i < hi && i >= lo && x[i] > mref[i] + 32.f &&
+                               mref[i] != -INFINITY;
+              const float f = fix ? ex2(mref[i] - x[i]) : 1.f;
+              if (__any_sync(0xffffffffu, fix)) {
+                for (int tp = 0; tp < t; ++tp) {
+                  const uint32_t ca = lane_addr + (uint32_t)(tp * NW + row0 + i);
+                  tmem_st1(ca, tmem_ld1(ca) * f);
+                }
+                tmem_wait_st();
+              }
             }
           }
-          __syncwarp();
+          if (need) {  // first visible token of a row, or the rare jump above
 #pragma unroll
-          for (int i = 0; i < kRPL; ++i) ms->sref[e][row_of<NW>(lane, i)] = mrun[i];
-          __syncwarp();
-#pragma unroll
-          for (int r = 0; r < NW; ++r) {
-            const bool vis = tv && r < W && tok <= prefix + r;
-            y[r] = vis ? ex2(x[r] - ms->sref[e][r]) : 0.f;
+            for (int i = 0; i < NH; ++i) {
+              if (i < hi && i >= lo && x[i] > mref[i] + 32.f) {
+                zsum[i] = mref[i] == -INFINITY ? 0.f : zsum[i] * ex2(mref[i] - x[i]);
+                mref[i] = x[i];
+              }
+            }
           }
-          reduce_rows<NW, false>(y, lane);
 #pragma unroll
-          for (int i = 0; i < kRPL; ++i) zrun[i] += y[i];
+          for (int i = 0; i < NH; ++i) {
+            x[i] = (i < hi && i >= lo) ? ex2(x[i] - mref[i]) : 0.f;
+            zsum[i] += x[i];
+          }
+          tmem_store_cols<NH>(lane_addr + (uint32_t)(t * NW + row0), x);
         }
+        tmem_wait_st();
+        float mkeep[NH];
+#pragma unroll
+        for (int i = 0; i < NH; ++i) mkeep[i] = mref[i];
         if (bad) record_status(a.status, KVSEL_ERR_NONFINITE);
         if (!ok) *abort_flag = 1;
-#pragma unroll
-        for (int i = 0; i < kRPL; ++i) {
-          if (NW != 16 || (lane & 1) == 0) {
-            ms->wm[e][row_of<NW>(lane, i)] = mrun[i];
-            ms->wz[e][row_of<NW>(lane, i)] = zrun[i];
-          }
+        reduce_stats<NH>(mref, zsum, lane);
+        constexpr int kLanesPerRow = 32 / NH;
+        if (lane % kLanesPerRow == 0) {
+          gs.wm[quarter][row0 + lane / kLanesPerRow] = mref[0];
+          gs.wz[quarter][row0 + lane / kLanesPerRow] = zsum[0];
         }
         // Control flow around the named barriers must be uniform across the
-        // epilogue, so decisions use values one thread published between
+        // group, so decisions use values one thread published between
         // barriers, never a direct read of the abort flag.
-        epi_bar();
-        if (et == 0) ms->snap = *abort_flag;
-        epi_bar();
-        const bool aborted = ms->snap != 0;
-        // ---- chunk statistics -> global partials
-        float* part = a.part + (int64_t)item * a.wpad * 2;
-        if (!aborted && et < W) {
-          float m = ms->wm[0][et], z = ms->wz[0][et];
-#pragma unroll
-          for (int w = 1; w < kEpiWarps; ++w) merge_stats(m, z, ms->wm[w][et], ms->wz[w][et]);
-          part[et * 2] = m;
-          part[et * 2 + 1] = z;
-          __threadfence();
-        }
-        epi_bar();
+        epi_bar(g);
         if (et == 0) {
-          int last = 0;
-          if (!aborted && !(a.inject == 1 && item == 0)) {
-            const int old = atomicAdd(a.counters + ip.inst, 1);
-            __threadfence();
-            last = old == a.seqs[ip.s].n_chunks - 1;
-          }
-          ms->is_last = last;
-          ms->timed_out = aborted ? 1 : 0;
+          gs.snap = *abort_flag;
+          gs.timed_out = gs.snap;
         }
-        epi_bar();
-        if (!aborted && ms->is_last) {
-          // merge every chunk of this instance, in chunk order per thread group
-          constexpr int tpr = kEpiThreads / NW;   // threads per row: 16, 8 or 4
+        epi_bar(g);
+        const bool aborted = gs.snap != 0;
+        // ---- chunk statistics: each row's (reference, sum) goes to this
+        // item's slot; then every chunk of the instance polls all the slots of
+        // the instance and merges them in the same fixed order
+        unsigned long long* slots = reinterpret_cast<unsigned long long*>(a.part);
+        if (!aborted && et < W) {
+          float m = gs.wm[0][et], z = gs.wz[0][et];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) merge_stats(m, z, gs.wm[w][et], gs.wz[w][et]);
+          if (m != m) m = INFINITY;  // keep the empty pattern unique (NONFINITE is recorded)
+          if (!(a.inject == 1 && item == 0))
+            slot_publish(slots + (int64_t)item * a.wpad + et, m, z);
+        }
+        const int nc = sd.n_chunks;
+        {
+          constexpr int tpr = kGroupThreads / NW;   // threads per row: 16, 8 or 4
+          constexpr int kPoll = 8;                  // slots read per batch
           const int r = et / tpr, sb = et % tpr;
-          const int nc = sd.n_chunks;
-          const int64_t item0 = (int64_t)ip.layer * a.items_per_layer + sd.item_base +
-                                (int64_t)ip.h * nc;
+          const unsigned long long* p0 =
+              slots + ((int64_t)ip.layer * a.items_per_layer + sd.item_base +
+                       (int64_t)ip.h * nc) * a.wpad + r;
           float m = -INFINITY, z = 0.f;
-          if (r < W) {
-            for (int c = sb; c < nc; c += tpr) {
-              const float* pc = a.part + ((item0 + c) * a.wpad + r) * 2;
-              merge_stats(m, z, __ldcg(pc), __ldcg(pc + 1));
+          bool late = false;
+          if (!aborted && r < W) {
+            const unsigned long long t0 = global_ns();
+            for (int cb = sb; cb < nc && !late; cb += kPoll * tpr) {
+              unsigned long long v[kPoll];
+              uint32_t pending = 0;
+#pragma unroll
+              for (int k = 0; k < kPoll; ++k) {
+                v[k] = kEmptySlot;
+                if (cb + k * tpr < nc) pending |= 1u << k;
+              }
+              for (;;) {
+#pragma unroll
+                for (int k = 0; k < kPoll; ++k) {
+                  if (pending & (1u << k)) {
+                    v[k] = slot_read(p0 + (int64_t)(cb + k * tpr) * a.wpad);
+                    if (v[k] != kEmptySlot) pending &= ~(1u << k);
+                  }
+                }
+                if (!pending) break;
+                if (global_ns() - t0 > limit) {
+                  late = true;
+                  break;
+                }
+                __nanosleep(64);
+              }
+#pragma unroll
+              for (int k = 0; k < kPoll; ++k)
+                if (!late && cb + k * tpr < nc)
+                  merge_stats(m, z, __uint_as_float((uint32_t)v[k]),
+                              __uint_as_float((uint32_t)(v[k] >> 32)));
             }
+          }
+          if (late) {
+            gs.timed_out = 1;
+            record_status(a.status, KVSEL_ERR_TIMEOUT);
           }
 #pragma unroll
           for (int off = tpr / 2; off >= 1; off >>= 1) {
@@ -590,64 +772,72 @@ __global__ void __launch_bounds__(kThreads, 1) tc_score_kernel(const __grid_cons
             const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
             merge_stats(m, z, m2, z2);
           }
-          if (sb == 0) {
-            const float f = r < W ? m + log2f(z) : INFINITY;
-            ms->fin[r] = f;
-            if (r < W) a.final_stats[(int64_t)ip.inst * a.wpad + r] = f;
-          }
-          __threadfence();
-          epi_bar();
-          if (et == 0) {
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.flags + ip.inst), "r"(1)
-                         : "memory");
-          }
-        } else if (!aborted) {
-          if (et == 0) {
-            const unsigned long long t0 = global_ns();
-            unsigned ns = 32;
-            int f = 0;
-            for (;;) {
-              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
-                           : "=r"(f)
-                           : "l"(a.flags + ip.inst)
-                           : "memory");
-              if (f) break;
-              if (global_ns() - t0 > limit) break;
-              __nanosleep(ns);
-              if (ns < 512) ns <<= 1;
-            }
-            if (!f) {
-              ms->timed_out = 1;
-              record_status(a.status, KVSEL_ERR_TIMEOUT);
-            }
-          }
-          epi_bar();
-          if (!ms->timed_out && et < NW)
-            ms->fin[et] = et < W ? __ldcg(a.final_stats + (int64_t)ip.inst * a.wpad + et)
-                                 : INFINITY;
+          if (sb == 0) gs.fin[r] = r < W ? m + log2f(z) : INFINITY;
         }
-        epi_bar();
-        // ---- pass C: votes from the logits still in TMEM
-        if (!ms->timed_out) {
-          for (int t = sub; t < ntiles; t += 2) {
-            float x[NW];
-            tmem_load_row<NW>(lane_addr + (uint32_t)(t * NW), x);
-            const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-            float vote = 0.f;
+        epi_bar(g);
+        // ---- pass C: vote of a prefix token = sum over rows of its stored
+        // exponential times c_r = 2^(reference_r - M_r - log2 Z_r). Each warp
+        // sums its half of the rows for every tile and leaves the partial in
+        // TMEM (in the first column of its half, already consumed); after a
+        // barrier of the warp pair, each warp adds the two partials of
+        // alternate tiles (half 0 first, a fixed order) and writes the votes.
+        if (!gs.timed_out) {
+          float c[NH];
 #pragma unroll
-            for (int r = 0; r < NW; ++r) vote += ex2(fmaf(x[r], a.scale_log2, -ms->fin[r]));
-            if (tok < sd.len) a.votes[plane + tok] = tok < prefix ? vote : 0.f;
+          for (int i = 0; i < NH; ++i) c[i] = ex2(mkeep[i] - gs.fin[row0 + i]);
+          constexpr int kB = NH <= 8 ? 2 : 1;  // tiles per batch of TMEM loads
+          for (int t0b = 0; t0b < ntiles; t0b += kB) {
+            float ev[kB * NH];
+#pragma unroll
+            for (int b = 0; b < kB; ++b)
+              if (t0b + b < ntiles)
+                tmem_load_cols_nowait<NH>(lane_addr + (uint32_t)((t0b + b) * NW + row0),
+                                          ev + b * NH);
+            tmem_wait_ld();
+            after_wait(ev);
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+              if (t0b + b < ntiles) {
+                float p = 0.f;
+#pragma unroll
+                for (int i = 0; i < NH; ++i) p = fmaf(ev[b * NH + i], c[i], p);
+                tmem_st1(lane_addr + (uint32_t)((t0b + b) * NW + row0), p);
+              }
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          pair_bar(g, quarter);
+          tc_fence_after();
+          constexpr int kHalfTiles = kTiles / 2;  // tiles finished by each warp of the pair
+          float pv[2 * kHalfTiles];
+#pragma unroll
+          for (int k = 0; k < kHalfTiles; ++k) {
+            const int t = sub + 2 * k;
+            if (t < ntiles) {
+              pv[2 * k] = tmem_ld1_nowait(lane_addr + (uint32_t)(t * NW));
+              pv[2 * k + 1] = tmem_ld1_nowait(lane_addr + (uint32_t)(t * NW + NH));
+            }
+          }
+          tmem_wait_ld();
+          after_wait(pv);
+#pragma unroll
+          for (int k = 0; k < kHalfTiles; ++k) {
+            const int t = sub + 2 * k;
+            const int tok = tok0 + t * kTileM + 32 * quarter + lane;
+            if (t < ntiles && tok < sd.len)
+              a.votes[plane + tok] = tok < prefix ? pv[2 * k] + pv[2 * k + 1] : 0.f;
           }
         }
-        if (et == 0 && ms->timed_out) *abort_flag = 1;
+        if (et == 0 && gs.timed_out) *abort_flag = 1;
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ms->tmem_empty));
+      if (lane == 0) mbar_arrive(smem_u32(&gs.tmem_empty));
       if constexpr (!LOGITS) {
-        if (et == 0) ms->snap = *abort_flag;
-        epi_bar();  // every epilogue thread has read ms->timed_out / fin
-        if (ms->snap) break;
+        if (et == 0) gs.snap = *abort_flag;
+        epi_bar(g);  // every thread of the group has read timed_out / fin
+        if (gs.snap) break;
       } else {
         if (!ok) break;
       }
@@ -733,7 +923,7 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   if (e) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(NW));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
@@ -771,10 +961,15 @@ int tc_window_pad(int W) {
 
 int tc_chunk_tokens(int W) {
   const int nw = tc_window_pad(W);
-  return nw ? kTileM * (kTmemCols / nw) : 0;
+  return nw ? kTileM * tiles_per_item(nw) : 0;
 }
 
 int tc_max_grid(int sm_count) { return sm_count; }
+
+int tc_max_chunks(int W, int sm_count) {
+  const int nw = tc_window_pad(W);
+  return nw ? groups_for(nw) * tc_max_grid(sm_count) : 0;
+}
 
 bool tc_eligible(int dtype, int D, int W, const void* q, const void* k) {
   if (dtype != KVSEL_BF16 || (D != 64 && D != 128) || tc_window_pad(W) == 0) return false;
