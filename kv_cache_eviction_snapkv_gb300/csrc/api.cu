@@ -189,6 +189,14 @@ kvsel_status check_budget(int W, int C) {
   return KVSEL_OK;
 }
 
+// Longest prefix among the sequences that are selected (L >= C).
+int64_t max_prefix(const Plan& p, int W, int C) {
+  int64_t m = 0;
+  for (const SeqDesc& s : p.all)
+    if (s.len >= C && s.len - W > m) m = s.len - W;
+  return m;
+}
+
 bool gen_supported(int W, int D) { return (int64_t)W * D <= kGenericMaxQ; }
 
 // Scoring plan: the scored sequences (all when C == 0, else L >= C) with
@@ -434,6 +442,7 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   if ((st = plan_shape(shape, C, &p))) return st;
   if ((st = check_window(p, W))) return st;
   if ((st = check_budget(W, C))) return st;
+  if (max_prefix(p, W, C) > kMaxPrefix) return KVSEL_ERR_UNSUPPORTED;
   if (p.T_out == 0) return KVSEL_OK;
   if (!pooled || !out_idx) return KVSEL_ERR_INVALID_ARG;
   DevState* d;
@@ -459,6 +468,7 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   sa.out_idx = out_idx;
   sa.status = d->status;
   sa.sm_count = d->sm_count;
+  sa.max_prefix = max_prefix(p, W, C);
   sa.stream = s;
   return cuda_fail(launch_select(sa), "selection launch");
 }
@@ -518,6 +528,7 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   if ((st = check_window(p, W))) return st;
   if ((st = check_budget(W, C))) return st;
   if ((st = check_pool(pool_kind, pool_k))) return st;
+  if (max_prefix(p, W, C) > kMaxPrefix) return KVSEL_ERR_UNSUPPORTED;
   if (p.T_out == 0) return KVSEL_OK;
   if (!q_win || !K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
   DevState* d;
@@ -554,34 +565,19 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   sa.out_idx = out_idx;
   sa.status = d->status;
   sa.sm_count = d->sm_count;
+  sa.max_prefix = max_prefix(p, W, C);
+  sa.gather = 1;
+  sa.k = K;
+  sa.v = V;
+  sa.out_k = out_K;
+  sa.out_v = out_V;
+  sa.row_bytes = (int64_t)p.D * p.elem_bytes;
   sa.stream = s;
-  if ((st = cuda_fail(launch_select(sa), "selection launch"))) return st;
-  if (ev) cudaEventRecord(ev[2], s);
-  CompactArgs ca{};
-  ca.k = K;
-  ca.v = V;
-  ca.idx = out_idx;
-  ca.out_k = out_K;
-  ca.out_v = out_V;
-  ca.layers = p.layers;
-  ca.H = p.H;
-  ca.S = p.S;
-  ca.C = C;
-  ca.T = p.T;
-  ca.T_out = p.T_out;
-  ca.row_bytes = (int64_t)p.D * p.elem_bytes;
-  ca.seqs = all_dev;
-  int64_t mr = 0;
-  for (const SeqDesc& q : p.all) {
-    const int64_t n = (int64_t)(q.len < C ? q.len : C) * p.H;
-    if (n > mr) mr = n;
+  if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
+  if (ev) {
+    cudaEventRecord(ev[2], s);
+    cudaEventRecord(ev[3], s);
   }
-  ca.max_rows = mr;
-  ca.status = d->status;
-  ca.sm_count = d->sm_count;
-  ca.stream = s;
-  if ((st = cuda_fail(launch_compact(ca), "gather launch"))) return st;
-  if (ev) cudaEventRecord(ev[3], s);
   return KVSEL_OK;
 }
 

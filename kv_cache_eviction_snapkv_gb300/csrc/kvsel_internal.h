@@ -71,6 +71,16 @@ struct SelectArgs {
   int32_t* out_idx;
   int* status;
   int sm_count;
+  int64_t max_prefix;      // largest L - W over the selected sequences
+  int cluster;             // CTAs per instance (set by the launcher)
+  int slice;               // prefix positions per CTA (set by the launcher)
+  int gather;              // 1: also copy the kept K/V rows (fused path)
+  const void* k;           // gather: K, V and the compacted outputs
+  const void* v;
+  void* out_k;
+  void* out_v;
+  int64_t row_bytes;       // gather: D * element bytes
+  int vec_bytes;           // gather: copy width (set by the launcher)
   cudaStream_t stream;
 };
 
@@ -91,6 +101,7 @@ struct CompactArgs {
 };
 
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
+constexpr int64_t kMaxPrefix = 262144;  // longest prefix L - W the select kernel takes
 constexpr int kGenericChunk = 256;   // tokens per CUDA-core scoring block
 constexpr int kGenericMaxQ = 16384;  // W * D floats staged in shared memory
 

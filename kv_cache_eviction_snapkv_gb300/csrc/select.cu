@@ -16,6 +16,8 @@
 // emit pass in position order takes every key > T and the first ones == T
 // (smaller positions first); an on-chip bitonic sort of (~key, position)
 // orders the kept positions by (-score, position).
+#include <algorithm>
+
 #include "kvsel_device.cuh"
 
 namespace kvsel {
@@ -24,6 +26,7 @@ namespace {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 2048;
+constexpr int kMaxCluster = 8;   // portable cluster size
 
 // Order-keeping key: larger float -> larger key; -0 == +0; NaN lowest.
 __device__ __forceinline__ uint32_t score_key(float v, int* status) {
@@ -65,26 +68,40 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
 
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 
-// Warp-aggregated histogram increment (all 32 lanes call it; kNoBin = skip).
+// Histogram increment from all 32 lanes (kNoBin = skip): one add of the
+// lane count when the whole warp shares a bin, else one add per lane.
 __device__ __forceinline__ void add_bin(uint32_t* hist, uint32_t bin, int lane) {
-  const unsigned peers = __match_any_sync(0xffffffffu, bin);
-  if (bin != kNoBin && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, 0);
+  if (__all_sync(0xffffffffu, bin == b0)) {
+    if (lane == 0 && b0 != kNoBin) atomicAdd(&hist[b0], 32u);
+  } else if (bin != kNoBin) {
+    atomicAdd(&hist[bin], 1u);
+  }
 }
 
-// Warp 0 finds the bin holding the krem-th largest key among the counted ones.
-// Writes (bin, count strictly above that bin) to out[0], out[1].
-__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t krem, uint32_t* out) {
-  const int lane = threadIdx.x & 31;
-  const int per = nbins / 32;
-  const int lo = lane * per;
+// All threads of the block: find the bin holding the krem-th largest key
+// among the counted ones; thread t owns bins [t*nb/NT, (t+1)*nb/NT). Writes
+// (bin, count strictly above that bin) to out[0], out[1]. `wsum` is scratch
+// for kSelWarps values. Ends with a barrier.
+__device__ void find_bin_block(const uint32_t* hist, int nb, uint32_t krem, uint32_t* out,
+                               uint32_t* wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nb / kSelThreads;           // 4 or 2
+  const int lo = tid * per;
   uint32_t mine = 0;
   for (int i = 0; i < per; ++i) mine += hist[lo + i];
-  uint32_t incl = mine;  // sum over lanes >= this lane
+  // suffix sums: bins owned by threads with a larger index come first
+  uint32_t incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+    const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
     if (lane + o < 32) incl += t;
   }
+  if (lane == 0) wsum[warp] = incl;           // the warp's total
+  __syncthreads();
+  uint32_t later = 0;
+  for (int w = warp + 1; w < kSelWarps; ++w) later += wsum[w];
+  incl += later;
   const uint32_t above = incl - mine;
   if (above < krem && krem <= incl) {
     uint32_t acc = above;
@@ -98,148 +115,455 @@ __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t krem, uint32_
       acc += c;
     }
   }
+  __syncthreads();
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a, int n2) {
+// ---------------------------------------------------------------------------
+// Cluster plumbing: CTA rank, cluster barrier, distributed shared memory
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (this CTA's shared memory) in the shared window of CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ void dsmem_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Ascending bitonic sort of n = nt * R u64 keys by the first nt threads of the
+// block, R per thread (thread t holds positions t*R .. t*R+R-1): strides below
+// R in registers, below 32R by warp shuffles, the rest through shared memory.
+// Every thread of the block calls it (the barriers need them all).
+// ---------------------------------------------------------------------------
+
+template <int R>
+__device__ void bitonic_sort_blocked(unsigned long long* buf, int nt) {
+  const int tid = threadIdx.x;
+  const bool mine = tid < nt;
+  const int n = nt * R;
+  const int base = tid * R;
+  unsigned long long v[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) v[r] = mine ? buf[base + r] : 0ull;
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32 * R) {
+        if (mine) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) buf[base + r] = v[r];
+        }
+        __syncthreads();
+        for (int i = tid; i < n / 2; i += blockDim.x) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const unsigned long long x = buf[lo], y = buf[hi];
+          if ((x > y) == up) {
+            buf[lo] = y;
+            buf[hi] = x;
+          }
+        }
+        __syncthreads();
+        if (mine) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) v[r] = buf[base + r];
+        }
+      } else if (mine) {
+        if (stride >= R) {
+          const int lx = stride / R;  // partner lane distance
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], lx);
+            const int e = base + r;
+            const bool up = (e & size) == 0;
+            const bool lower = (e & stride) == 0;
+            const unsigned long long mn = v[r] < o ? v[r] : o, mx = v[r] < o ? o : v[r];
+            v[r] = (lower == up) ? mn : mx;
+          }
+        } else {
+          // dispatch to a compile-time stride so the array is indexed statically
+#pragma unroll
+          for (int cs = R / 2; cs >= 1; cs >>= 1) {
+            if (cs == stride) {
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                if ((r & cs) == 0) {
+                  const bool up = ((base + r) & size) == 0;
+                  if ((v[r] > v[r | cs]) == up) {
+                    const unsigned long long t = v[r];
+                    v[r] = v[r | cs];
+                    v[r | cs] = t;
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  if (mine) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) buf[base + r] = v[r];
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// The selection kernel: one cluster of CS CTAs per (layer, sequence, head).
+// CTA `rank` owns prefix positions [rank * NT*E, (rank+1) * NT*E) and keeps
+// their keys in registers (position j = slice start + i*NT + tid for
+// i < E). Histograms are summed in the leader (rank 0) through distributed
+// shared memory; the leader sorts the kept keys and writes the output.
+// ---------------------------------------------------------------------------
+
+struct SelShared {
+  uint32_t hist[kBins];        // this CTA's histogram
+  uint32_t ghist[kBins];       // leader: the cluster's histogram
+  uint32_t res[2];             // leader: (bin, count above)
+  uint32_t cnt[kMaxCluster][2];  // leader: per rank (greater, equal) counts
+  uint32_t warp_cnt[kSelWarps][2];
+  uint32_t wsum[kSelWarps];
+};
+
+// Pooled score at stage position c of a zero-padded stage (s[c - R] ..
+// s[c + R] are in bounds): sum in increasing position order, then / k
+// (adding the zero pads leaves the sum unchanged); or the max.
+template <int K>
+__device__ __forceinline__ float pool_fixed(const float* s, int c, int kind) {
+  constexpr int R = K / 2;
+  if (kind == KVSEL_POOL_AVG) {
+    float acc = 0.f;
+#pragma unroll
+    for (int d = -R; d <= R; ++d) acc += s[c + d];
+    return acc / (float)K;
+  }
+  float m = s[c - R];
+#pragma unroll
+  for (int d = -R + 1; d <= R; ++d) m = fmaxf(m, s[c + d]);
+  return m;
+}
+
+__device__ __forceinline__ float pool_any(const float* s, int c, int kind, int k) {
+  switch (k) {
+    case 1: return s[c];
+    case 3: return pool_fixed<3>(s, c, kind);
+    case 5: return pool_fixed<5>(s, c, kind);
+    case 7: return pool_fixed<7>(s, c, kind);
+    case 9: return pool_fixed<9>(s, c, kind);
+    default: {
+      const int R = k >> 1;
+      if (kind == KVSEL_POOL_AVG) {
+        float acc = 0.f;
+        for (int d = -R; d <= R; ++d) acc += s[c + d];
+        return acc / (float)k;
+      }
+      float m = s[c - R];
+      for (int d = -R + 1; d <= R; ++d) m = fmaxf(m, s[c + d]);
+      return m;
+    }
+  }
+}
+
+constexpr int kMaxE = 32;  // slice positions per thread of one CTA
+
+template <int VW> struct CopyVec;
+template <> struct CopyVec<16> { using T = uint4; };
+template <> struct CopyVec<8> { using T = uint2; };
+template <> struct CopyVec<4> { using T = uint32_t; };
+template <> struct CopyVec<2> { using T = uint16_t; };
+
+// Copies the instance's kept K and V rows (slot s <- position idx(s)) into
+// out_K / out_V with VW-byte vectors, several rows in flight per thread.
+template <int VW, typename IdxOf>
+__device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int64_t src_tok0,
+                                            int64_t dst_row0, int h, IdxOf idx_of) {
+  using V = typename CopyVec<VW>::T;
+  constexpr int kU = 4;
+  const int vpr = (int)(a.row_bytes / VW);
+  const int total = n_rows * vpr;
+  const char* kb = reinterpret_cast<const char*>(a.k);
+  const char* vb = reinterpret_cast<const char*>(a.v);
+  char* okb = reinterpret_cast<char*>(a.out_k);
+  char* ovb = reinterpret_cast<char*>(a.out_v);
+  for (int e0 = threadIdx.x; e0 < total; e0 += kSelThreads * kU) {
+    V kv[kU], vv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kSelThreads;
+      if (e < total) {
+        const int s = e / vpr, vi = e - s * vpr;
+        const int64_t src = ((src_tok0 + idx_of(s)) * a.H + h) * a.row_bytes + (int64_t)vi * VW;
+        kv[u] = __ldcs(reinterpret_cast<const V*>(kb + src));
+        vv[u] = __ldcs(reinterpret_cast<const V*>(vb + src));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kSelThreads;
+      if (e < total) {
+        const int s = e / vpr, vi = e - s * vpr;
+        const int64_t dst = ((dst_row0 + s) * a.H + h) * a.row_bytes + (int64_t)vi * VW;
+        __stcs(reinterpret_cast<V*>(okb + dst), kv[u]);
+        __stcs(reinterpret_cast<V*>(ovb + dst), vv[u]);
+      }
+    }
+  }
+}
+
+template <typename IdxOf>
+__device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int64_t src_tok0,
+                                           int64_t dst_row0, int h, IdxOf idx_of) {
+  switch (a.vec_bytes) {
+    case 16: gather_rows<16>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
+    case 8: gather_rows<8>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
+    case 4: gather_rows<4>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
+    default: gather_rows<2>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
+  }
+}
+
+// One cluster of CS CTAs per (layer, sequence, head): CTA `rank` owns prefix
+// positions [rank * slice, (rank+1) * slice). Dynamic shared memory: stage |
+// sortbuf. `stage` holds the slice's votes with a zero halo of pool_k / 2 on
+// each side, and the slice's keys are written over it; the leader's
+// `sortbuf` receives every kept key of the cluster. With `a.gather` the
+// leader also copies the kept K/V rows (the fused path).
+template <int R>
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + kBins * 4);
-  __shared__ uint32_t found[2];
-  __shared__ uint32_t warp_eq[kSelWarps];
-  __shared__ uint32_t n_sel;
+  __shared__ SelShared sh;
+  const int pad = a.pool_inline ? (a.pool_k >> 1) : 0;
+  float* stage = reinterpret_cast<float*>(smem);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  unsigned long long* sortbuf = reinterpret_cast<unsigned long long*>(
+      smem + ((((size_t)a.slice + 2 * pad) * 4 + 15) & ~size_t(15)));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int inst = blockIdx.x;                 // ((layer * S) + b) * H + h
+  const uint32_t rank = cluster_rank();
+  const int cs = a.cluster;
+  const int inst = blockIdx.x / cs;            // ((layer * S) + b) * H + h
   const int h = inst % a.H;
   const int lb = inst / a.H;
   const int b = lb % a.n_seqs;
   const int layer = lb / a.n_seqs;
   const SeqDesc sd = a.seqs[b];
   const int L = sd.len;
-  int32_t* out = a.out_idx + ((int64_t)layer * a.T_out + sd.out_off) * a.H + h;
+  const int64_t out_row0 = (int64_t)layer * a.T_out + sd.out_off;
+  int32_t* out = a.out_idx + out_row0 * a.H + h;
+  const int64_t src_tok0 = (int64_t)layer * a.T + sd.tok_off;
 
-  if (L < a.C) {  // bypass: keep everything in order
-    for (int s = tid; s < L; s += kSelThreads) out[(int64_t)s * a.H] = s;
+  if (L < a.C) {  // bypass: keep everything in order (uniform over the cluster)
+    if (rank == 0) {
+      for (int s = tid; s < L; s += kSelThreads) out[(int64_t)s * a.H] = s;
+      if (a.gather) gather_any(a, L, src_tok0, out_row0, h, [](int s) { return s; });
+    }
     return;
   }
   const int P = L - a.W;
   const uint32_t k = (uint32_t)(a.C - a.W);
+  const int j0 = (int)rank * a.slice;                  // slice start
+  const int j1 = min(P, j0 + a.slice);                 // slice end (may be <= j0)
+  const int n = max(0, j1 - j0);
   const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sd.tok_off;
   const float* src = a.scores + plane;
-  const float* sc = src;  // the scores the passes read
 
-  // Pass 1 (with pooling when inline): histogram of the top 11 key bits.
-  for (int i = tid; i < kBins; i += kSelThreads) hist[i] = 0;
-  __syncthreads();
-  float* pl = a.pooled_ws + plane;
-  for (int base = 0; base < P; base += kSelThreads) {
-    const int j = base + tid;
-    uint32_t bin = kNoBin;
-    if (j < P) {
-      float v;
-      if (a.pool_inline) {
-        v = pool_at(src, j, P, a.pool_kind, a.pool_k);
-        pl[j] = v;
-      } else {
-        v = src[j];
-      }
-      bin = score_key(v, a.status) >> 21;
-    }
-    add_bin(hist, bin, lane);
-  }
-  if (a.pool_inline) sc = pl;
-  __syncthreads();
-  if (warp == 0) find_bin(hist, kBins, k, found);
-  __syncthreads();
-  const uint32_t d1 = found[0];
-  uint32_t krem = k - found[1];
+  const uint32_t ghist_r = dsmem_addr(sh.ghist, 0);
+  const uint32_t res_r = dsmem_addr(sh.res, 0);
+  const uint32_t cnt_r = dsmem_addr(sh.cnt, 0);
+  const uint32_t sort_r = dsmem_addr(sortbuf, 0);
 
-  // Pass 2: next 11 bits among keys whose top 11 bits are d1.
-  for (int i = tid; i < kBins; i += kSelThreads) hist[i] = 0;
-  __syncthreads();
-  for (int base = 0; base < P; base += kSelThreads) {
-    const int j = base + tid;
-    uint32_t bin = kNoBin;
-    if (j < P) {
-      const uint32_t key = score_key(sc[j], a.status);
-      if ((key >> 21) == d1) bin = (key >> 10) & 0x7FFu;
-    }
-    add_bin(hist, bin, lane);
+  // ---- keys: stage the scores (with the zero halo), then, chunk by chunk,
+  // read each position's window and write its key at stage index j - j0,
+  // which only overwrites votes no later window needs.
+  for (int c = tid; c < n + 2 * pad; c += kSelThreads) {
+    const int j = j0 - pad + c;
+    stage[c] = (j >= 0 && j < P) ? src[j] : 0.f;
   }
   __syncthreads();
-  if (warp == 0) find_bin(hist, kBins, krem, found);
-  __syncthreads();
-  const uint32_t d2 = found[0];
-  krem -= found[1];
-
-  // Pass 3: last 10 bits among keys whose top 22 bits are (d1, d2).
-  const uint32_t top22 = (d1 << 11) | d2;
-  for (int i = tid; i < 1024; i += kSelThreads) hist[i] = 0;
-  __syncthreads();
-  for (int base = 0; base < P; base += kSelThreads) {
-    const int j = base + tid;
-    uint32_t bin = kNoBin;
-    if (j < P) {
-      const uint32_t key = score_key(sc[j], a.status);
-      if ((key >> 10) == top22) bin = key & 0x3FFu;
+  for (int c0 = 0; c0 < n; c0 += kSelThreads) {
+    const int i = c0 + tid;
+    uint32_t key = 0u;
+    if (i < n) {
+      const float v = a.pool_inline ? pool_any(stage, i + pad, a.pool_kind, a.pool_k) : stage[i];
+      key = score_key(v, a.status);
     }
-    add_bin(hist, bin, lane);
-  }
-  __syncthreads();
-  if (warp == 0) find_bin(hist, 1024, krem, found);
-  __syncthreads();
-  const uint32_t thr = (top22 << 10) | found[0];
-  const uint32_t need_eq = krem - found[1];  // keys == thr to keep, smallest positions first
-
-  // Emit pass in position order.
-  if (tid == 0) n_sel = 0;
-  uint32_t eq_base = 0;
-  __syncthreads();
-  for (int base = 0; base < P; base += kSelThreads) {
-    const int j = base + tid;
-    const uint32_t key = j < P ? score_key(sc[j], a.status) : 0u;
-    const bool gt = j < P && key > thr;
-    const bool eq = j < P && key == thr;
-    const uint32_t bal = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) warp_eq[warp] = __popc(bal);
     __syncthreads();
-    uint32_t before = eq_base, total = 0;
-#pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) {
-      const uint32_t c = warp_eq[w];
-      if (w < warp) before += c;
-      total += c;
-    }
-    before += __popc(bal & ((1u << lane) - 1u));
-    if (gt || (eq && before < need_eq)) {
-      const uint32_t pos = atomicAdd(&n_sel, 1u);
-      keys[pos] = ((unsigned long long)(~key) << 32) | (uint32_t)j;
-    }
-    eq_base += total;
-    __syncthreads();
+    if (i < n) keys[i] = key;
   }
-  for (int i = (int)k + tid; i < n2; i += kSelThreads) keys[i] = ~0ull;
+  if (rank == 0)
+    for (int i = tid; i < kBins; i += kSelThreads) sh.ghist[i] = 0;
   __syncthreads();
+  cluster_sync();
 
-  // Bitonic sort ascending: larger score first, then smaller position.
-  for (int size = 2; size <= n2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < (n2 >> 1); i += kSelThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long x = keys[lo], y = keys[hi];
-        if ((x > y) == up) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
+  // ---- three radix passes over (11, 11, 10) bits, summed in the leader
+  uint32_t krem = k, prefix = 0;
+  const int n_up = (n + kSelThreads - 1) / kSelThreads * kSelThreads;  // warp-uniform trips
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+    const int nb = pass == 2 ? 1024 : kBins;
+    const int hi_shift = pass == 0 ? 32 : pass == 1 ? 21 : 10;
+    for (int i = tid; i < nb; i += kSelThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_up; i += kSelThreads) {
+      uint32_t bin = kNoBin;
+      if (i < n) {
+        const uint32_t key = keys[i];
+        if (pass == 0 || (key >> hi_shift) == prefix) bin = (key >> shift) & (uint32_t)(nb - 1);
       }
+      add_bin(sh.hist, bin, lane);
+    }
+    __syncthreads();
+    for (int i = tid; i < nb; i += kSelThreads)
+      if (sh.hist[i]) dsmem_add_u32(ghist_r + 4u * i, sh.hist[i]);
+    cluster_sync();
+    if (rank == 0) {
+      find_bin_block(sh.ghist, nb, krem, sh.res, sh.wsum);
+      for (int i = tid; i < nb; i += kSelThreads) sh.ghist[i] = 0;
+    }
+    cluster_sync();
+    const uint32_t d = dsmem_ld_u32(res_r), above = dsmem_ld_u32(res_r + 4);
+    prefix = (prefix << (pass == 2 ? 10 : 11)) | d;
+    krem -= above;
+  }
+  const uint32_t thr = prefix;      // the key of the (C - W)-th largest score
+  const uint32_t need_eq = krem;    // how many keys equal to thr are kept
+
+  // ---- counts of this slice, exchanged through the leader
+  uint32_t my_gt = 0, my_eq = 0;
+  for (int i = tid; i < n; i += kSelThreads) {
+    const uint32_t key = keys[i];
+    my_gt += key > thr;
+    my_eq += key == thr;
+  }
+  my_gt = __reduce_add_sync(0xffffffffu, my_gt);
+  my_eq = __reduce_add_sync(0xffffffffu, my_eq);
+  if (lane == 0) {
+    sh.warp_cnt[warp][0] = my_gt;
+    sh.warp_cnt[warp][1] = my_eq;
+  }
+  __syncthreads();
+  uint32_t slice_gt = 0, slice_eq = 0;
+  for (int w = 0; w < kSelWarps; ++w) {
+    slice_gt += sh.warp_cnt[w][0];
+    slice_eq += sh.warp_cnt[w][1];
+  }
+  if (tid == 0) {
+    dsmem_st_u32(cnt_r + 8u * rank, slice_gt);
+    dsmem_st_u32(cnt_r + 8u * rank + 4u, slice_eq);
+  }
+  cluster_sync();
+  uint32_t eq_base = 0, sel_base = 0, take_eq = 0;
+  for (int r = 0; r <= (int)rank; ++r) {
+    const uint32_t g = dsmem_ld_u32(cnt_r + 8u * r), q = dsmem_ld_u32(cnt_r + 8u * r + 4u);
+    const uint32_t take = need_eq > eq_base ? min(q, need_eq - eq_base) : 0u;
+    if (r == (int)rank) {
+      take_eq = take;
+    } else {
+      sel_base += g + take;
+      eq_base += q;
+    }
+  }
+  // equal keys of this slice to keep: the first take_eq in position order
+  const bool all_eq = take_eq == slice_eq;
+  __syncthreads();  // warp_cnt is reused below
+
+  // ---- emit kept keys (composite ~key << 32 | position) into the leader.
+  // Phase 1 marks kept keys (bit m of `mask` for slice index tid + m*NT) and
+  // counts them per warp; phase 2 writes them at consecutive places.
+  uint32_t mask = 0, eq_seen = 0;
+  if (all_eq || take_eq == 0) {
+    for (int m = 0, i = tid; m < kMaxE && i < n; ++m, i += kSelThreads) {
+      const uint32_t key = keys[i];
+      if (key > thr || (all_eq && key == thr)) mask |= 1u << m;
+    }
+  } else {
+    // the straddling slice: rank equal keys in position order, row by row
+    for (int m = 0; m < kMaxE && m * kSelThreads < n; ++m) {
+      const int i = tid + m * kSelThreads;
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool eq = i < n && key == thr;
+      const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) sh.warp_cnt[warp][1] = __popc(bal);
+      __syncthreads();
+      uint32_t before = eq_seen, row = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        const uint32_t c = sh.warp_cnt[w][1];
+        if (w < warp) before += c;
+        row += c;
+      }
+      before += __popc(bal & ((1u << lane) - 1u));
+      if ((i < n && key > thr) || (eq && before < take_eq)) mask |= 1u << m;
+      eq_seen += row;
       __syncthreads();
     }
   }
+  const uint32_t mine = __popc(mask);
+  const uint32_t warp_total = __reduce_add_sync(0xffffffffu, mine);
+  if (lane == 0) sh.warp_cnt[warp][0] = warp_total;
+  __syncthreads();
+  uint32_t pos = sel_base;
+  for (int w = 0; w < warp; ++w) pos += sh.warp_cnt[w][0];
+  uint32_t incl = mine;  // inclusive prefix of `mine` over the warp's lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  pos += incl - mine;
+  for (int i = tid; mask; i += kSelThreads) {
+    if (mask & 1u) {
+      dsmem_st_u64(sort_r + 8u * pos, ((unsigned long long)(~keys[i]) << 32) | (uint32_t)(j0 + i));
+      ++pos;
+    }
+    mask >>= 1;
+  }
+  cluster_sync();
+  if (rank != 0) return;
+
+  // ---- leader: sort (larger score first, then smaller position), write the
+  // slots, then (fused path) copy the kept K/V rows
+  const int n2 = kSelThreads * R;
+  for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort_blocked<R>(sortbuf, kSelThreads);
   for (int s = tid; s < (int)k; s += kSelThreads)
-    out[(int64_t)s * a.H] = (int32_t)(keys[s] & 0xFFFFFFFFull);
+    out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
   for (int w = tid; w < a.W; w += kSelThreads) out[(int64_t)(k + w) * a.H] = P + w;
+  if (a.gather) {
+    const int kk = (int)k;
+    gather_any(a, a.C, src_tok0, out_row0, h, [&](int s) {
+      return s < kk ? (int)(sortbuf[s] & 0xFFFFFFFFull) : P + (s - kk);
+    });
+  }
 }
 
 }  // namespace
@@ -251,18 +575,58 @@ cudaError_t launch_pool(const PoolArgs& a) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const SelectArgs& a) {
-  const int64_t blocks = (int64_t)a.layers * a.n_seqs * a.H;
+cudaError_t launch_select(const SelectArgs& a0) {
+  const int64_t blocks = (int64_t)a0.layers * a0.n_seqs * a0.H;
   if (blocks == 0) return cudaSuccess;
-  int n2 = 1;
+  SelectArgs a = a0;
+  // one CTA per instance up to kSelThreads * kMaxE prefix positions, else a
+  // cluster of CTAs with equal slices
+  const int64_t cap = (int64_t)kSelThreads * kMaxE;
+  int cs = (int)((a.max_prefix + cap - 1) / cap);
+  if (cs < 1) cs = 1;
+  if (cs > kMaxCluster) return cudaErrorInvalidValue;
+  a.cluster = cs;
+  a.slice = (int)((a.max_prefix + cs - 1) / cs);
+  if (a.slice < 1) a.slice = 1;
+  int n2 = kSelThreads;
   while (n2 < a.C - a.W) n2 <<= 1;
-  if (n2 < 2) n2 = 2;
-  const size_t smem = kBins * 4 + (size_t)n2 * 8;
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const int pad = a.pool_inline ? a.pool_k / 2 : 0;
+  const size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
+  const size_t smem = stage + (size_t)n2 * 8;
+  void (*kern)(SelectArgs) = nullptr;
+  switch (n2 / kSelThreads) {
+    case 1: kern = select_kernel<1>; break;
+    case 2: kern = select_kernel<2>; break;
+    case 4: kern = select_kernel<4>; break;
+    case 8: kern = select_kernel<8>; break;
+    case 16: kern = select_kernel<16>; break;
+    case 32: kern = select_kernel<32>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (a.gather) {
+    auto ok = [&](int vw) {
+      if (a.row_bytes % vw) return false;
+      for (const void* p : {a.k, a.v, (const void*)a.out_k, (const void*)a.out_v})
+        if (reinterpret_cast<uintptr_t>(p) % vw) return false;
+      return true;
+    };
+    a.vec_bytes = ok(16) ? 16 : ok(8) ? 8 : ok(4) ? 4 : 2;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
-  select_kernel<<<(unsigned)blocks, kSelThreads, smem, a.stream>>>(a, n2);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(blocks * cs));
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace kvsel
