@@ -131,6 +131,24 @@ kvsel_status kvsel_score(const kvsel_shape* shape, const void* q_win, const void
                          int32_t pool_kind, int32_t pool_k, float* votes, float* pooled,
                          void* stream);
 
+/* kvsel_score without any device allocation, for callers that cannot call
+ * cudaMalloc (an allocator they must not bypass, or a context where
+ * allocating is not permitted). The paper has no counterpart; it is a
+ * deployment variant of kvsel_score with the same arguments, rules and
+ * results, except that votes must be non-NULL (the caller provides it).
+ * Scratch: a fixed 8 MiB array in device memory, part of the library image
+ * (every GPU that loads the library holds it until the process exits). The
+ * first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture. Calls whose scratch need exceeds 8 MiB (roughly: layers x heads x
+ * ceil(L / 1024) x W x 8 bytes summed over sequences, plus small tables)
+ * return KVSEL_ERR_UNSUPPORTED and launch nothing. All calls on a device share
+ * the array and each call resets what must start out empty, so calls that
+ * overlap on the GPU (different streams without ordering) race. */
+kvsel_status kvsel_score_static(const kvsel_shape* shape, const void* q_win, const void* K,
+                                int32_t W, int32_t pool_kind, int32_t pool_k, float* votes,
+                                float* pooled, void* stream);
+
 /* Top-(C - W) selection from given pooled scores ([num_layers][H][T] fp32,
  * only prefix entries are read) into out_idx ([num_layers][T_out][H] int32);
  * bypass sequences (L < C) get 0..L-1. Ordering of scores: IEEE order with

@@ -148,6 +148,26 @@ def kvsel_score(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: int,
     return votes, pooled
 
 
+def kvsel_score_static(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: int,
+                       votes=None, pooled=None, stream=None):
+    """kvsel_score that allocates no device memory inside the library (its
+    scratch is a fixed array in the library image); the output tensors are
+    still the caller's."""
+    sh = shape_of(K, seq_offsets)
+    K4, q4 = _as4(K), _as4(q_win)
+    _need(K4, "K"), _need(q4, "q_win", K4.dtype)
+    L, _, H, _ = K4.shape
+    if votes is None:
+        votes = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
+    if pooled is None:
+        pooled = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
+    _need(votes, "votes", torch.float32), _need(pooled, "pooled", torch.float32)
+    _check(_native.lib().kvsel_score_static(sh.ref, _ptr(q4), _ptr(K4), int(W), int(pool_kind),
+                                            int(pool_k), _ptr(votes), _ptr(pooled),
+                                            _stream(stream)), "kvsel_score_static")
+    return votes, pooled
+
+
 def kvsel_select(pooled, seq_offsets, num_heads: int, W: int, C: int, out_idx=None,
                  stream=None):
     """out_idx [layers, T_out, H] int32 from pooled scores [layers, H, T]."""

@@ -332,6 +332,105 @@ size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
 }  // namespace
 }  // namespace kvsel
 
+// ---------------------------------------------------------------------------
+// kvsel_score_static: kvsel_score for callers that cannot allocate device
+// memory, for instance code that runs under an allocator it must not bypass
+// or in a context where cudaMalloc is not permitted. Its scratch (sequence
+// tables, the cross-chunk exchange slots, merged row statistics) lives in a
+// file-scope device array instead of the cudaMalloc'd workspace. Every GPU
+// that loads the library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace kvsel {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+char* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device; looked up once
+// per device (the host-side name is only a stand-in for the device symbol).
+kvsel_status static_scratch(char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return KVSEL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)))
+      return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = static_cast<char*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return KVSEL_OK;
+}
+
+// Scratch bytes kvsel_score_static carves, in the order it carves them.
+size_t static_score_bytes(const Plan& p, const ScorePlan& sp) {
+  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
+  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
+  Carve c;
+  c.take(p.all.size() * sizeof(SeqDesc) + 1);                 // every sequence
+  c.take(sp.scored.size() * sizeof(SeqDesc));                 // scored sequences
+  c.take((size_t)items * sp.wpad * 2 * sizeof(float));        // exchange slots / partials
+  c.take((size_t)insts * 2 * sizeof(int));                    // counters
+  c.take((size_t)insts * sp.wpad * sizeof(float));            // merged statistics
+  return c.off;
+}
+
+}  // namespace
+
+}  // namespace kvsel
+
+extern "C" kvsel_status kvsel_score_static(const kvsel_shape* shape, const void* q_win,
+                                           const void* K, int32_t W, int32_t pool_kind,
+                                           int32_t pool_k, float* votes, float* pooled,
+                                           void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_pool(pool_kind, pool_k))) return st;
+  if (p.T == 0) return KVSEL_OK;
+  if (!q_win || !K || !votes || !pooled) return KVSEL_ERR_INVALID_ARG;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  ScorePlan sp;
+  if ((st = plan_score(p, W, 0, q_win, K, d, &sp))) return st;
+  const size_t need = static_score_bytes(p, sp);
+  if (need > kStaticScratchBytes) {
+    std::fprintf(stderr,
+                 "libkvsel: kvsel_score_static needs %zu scratch bytes, more than its "
+                 "fixed %zu; use kvsel_score\n",
+                 need, kStaticScratchBytes);
+    return KVSEL_ERR_UNSUPPORTED;
+  }
+  char* ws;
+  if ((st = static_scratch(&ws))) return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s))) return st;
+  PoolArgs pa{};
+  pa.votes = votes;
+  pa.pooled = pooled;
+  pa.layers = p.layers;
+  pa.H = p.H;
+  pa.W = W;
+  pa.pool_kind = pool_kind;
+  pa.pool_k = pool_k;
+  pa.T = p.T;
+  pa.n_seqs = p.S;
+  pa.seqs = all_dev;
+  pa.stream = s;
+  return cuda_fail(launch_pool(pa), "pooling launch");
+}
+
 using namespace kvsel;
 
 extern "C" {
