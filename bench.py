@@ -210,6 +210,27 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------
 
+def score_traffic(layers_full: int):
+    """DRAM bytes per full launch of the scoring kernel from the committed ncu
+    summary, scaled from the captured layer count; None when the kernel source
+    changed since the capture (its sha256 is recorded beside the counters)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "score_tc_cfg2_ncu.md")
+    src = os.path.join(ROOT, "kv_cache_eviction_snapkv_gb300", "csrc", "score_tc.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("source_sha256:", "dram_bytes_per_launch:",
+                                      "captured_layers:")))
+    if fields.get("source_sha256", "").strip() != digest:
+        return None
+    per_capture = float(fields["dram_bytes_per_launch"])
+    return per_capture * layers_full / float(fields["captured_layers"])
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -243,9 +264,11 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
 
+    from kv_cache_eviction_snapkv_gb300 import shard
     wl = wk.make_workload(args.config)
     if args.layers:
         wl.layers = args.layers
+    wl.seed = shard.rank_seed(wl.seed, rank)   # rank r's own batch (weak scaling)
     q, k, v = wk.device_tensors(wl, dev)
     shape = api.shape_of(k, wl.offsets)
     t_out = api.kvsel_out_tokens(shape, wl.capacity)
@@ -282,11 +305,7 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = shard.max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
 
     # Stage durations (events recorded by the library on this stream).
     n_prof = max(3, min(args.steps, 100))
@@ -339,11 +358,7 @@ def main():
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = ev0.elapsed_time(ev1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = shard.max_over_ranks(ev0.elapsed_time(ev1) / args.e2e_steps, dev)
         nbytes = lambda t: t.numel() * t.element_size()
         e2e = {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
@@ -360,7 +375,7 @@ def main():
                "sample": cpu_pool.sample_text()}
 
     if rank == 0:
-        launches_per_step = 3 if path == 1 else 5
+        launches_per_step = 2 if path == 1 else 4   # score kernel(s) + select/gather
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -373,10 +388,11 @@ def main():
                          "statistics, votes)" if path == 1 else "generic scoring kernels",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": None, "bytes_per_launch": score_bytes,
+                         "traffic": score_traffic(wl.layers) if path == 1 else None,
+                         "bytes_per_launch": score_bytes,
                          "avg_launch_ms": score_ms},
-            "stages_ms": {"score": stage_ms[0] / calls, "select": stage_ms[1] / calls,
-                          "gather": stage_ms[2] / calls, "calls": calls},
+            "stages_ms": {"score": stage_ms[0] / calls, "select_gather": stage_ms[1] / calls,
+                          "calls": calls},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
