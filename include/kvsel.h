@@ -191,8 +191,8 @@ kvsel_status kvsel_set_wait_limit_ns(uint64_t ns);
 kvsel_status kvsel_debug_inject(int32_t what);
 
 /* Stage timing of kvsel_snapkv with CUDA events recorded on the caller's
- * stream around each stage: [0] scoring kernel(s), [1] selection kernel,
- * [2] gather kernel. kvsel_profile_begin(n) arms it for the next n calls on
+ * stream around each stage: [0] scoring kernel(s), [1] selection with the
+ * fused K/V gather, [2] unused (0; the gather runs inside stage [1]). kvsel_profile_begin(n) arms it for the next n calls on
  * the current device (n in 1..100000; creates the events); each call records
  * its events without synchronising. kvsel_profile_end() synchronises, writes
  * the summed milliseconds per stage to stage_ms[0..2] and the number of
