@@ -229,8 +229,8 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
   };
   if (tc_ok) {
     build(tc_chunk_tokens(W));
-    // the waits between the chunks of one instance end only if every chunk
-    // can be in flight at once (chunks <= CTAs x TMEM buffers per CTA)
+    // the waits between the chunks of one instance end only if its chunks
+    // span at most three rounds of items (chunks <= 2 x CTAs)
     if (sp->max_chunks <= tc_max_chunks(W, d->sm_count)) {
       sp->tc = true;
       sp->chunk = tc_chunk_tokens(W);
@@ -257,7 +257,7 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
   const size_t o_seq = cv.take(sp.scored.size() * sizeof(SeqDesc));
   const size_t o_part = cv.take((size_t)items * sp.wpad * 2 * sizeof(float));
   const size_t o_cnt = cv.take((size_t)insts * 2 * sizeof(int));
-  const size_t o_fin = cv.take((size_t)insts * sp.wpad * sizeof(float));
+  const size_t o_fin = cv.take((size_t)insts * sp.wpad * 2 * sizeof(float));
   cudaError_t e = cudaMemcpyAsync(ws + o_seq, sp.scored.data(),
                                   sp.scored.size() * sizeof(SeqDesc),
                                   cudaMemcpyHostToDevice, stream);
@@ -299,6 +299,9 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
     // the tensor-core kernel's exchange slots start out as all-ones (empty)
     if ((e = cudaMemsetAsync(a.part, 0xFF, (size_t)items * sp.wpad * 2 * sizeof(float), stream)))
       return cuda_fail(e, "cudaMemsetAsync(exchange slots)");
+    if ((e = cudaMemsetAsync(a.final_stats, 0xFF, (size_t)insts * sp.wpad * 2 * sizeof(float),
+                             stream)))
+      return cuda_fail(e, "cudaMemsetAsync(final slots)");
     int grid = tc_max_grid(d->sm_count);
     if (items < grid) grid = (int)items;
     if (ev) cudaEventRecord(ev[0], stream);
@@ -326,7 +329,7 @@ size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
   const int64_t items = (int64_t)p.layers * sp.items_per_layer;
   const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
   return 4096 + sp.scored.size() * sizeof(SeqDesc) + (size_t)items * sp.wpad * 8 +
-         (size_t)insts * 8 + (size_t)insts * sp.wpad * 4 + 4 * 256;
+         (size_t)insts * 8 + (size_t)insts * sp.wpad * 8 + 4 * 256;
 }
 
 }  // namespace
@@ -377,7 +380,7 @@ size_t static_score_bytes(const Plan& p, const ScorePlan& sp) {
   c.take(sp.scored.size() * sizeof(SeqDesc));                 // scored sequences
   c.take((size_t)items * sp.wpad * 2 * sizeof(float));        // exchange slots / partials
   c.take((size_t)insts * 2 * sizeof(int));                    // counters
-  c.take((size_t)insts * sp.wpad * sizeof(float));            // merged statistics
+  c.take((size_t)insts * sp.wpad * 2 * sizeof(float));        // merged statistics / slots
   return c.off;
 }
 

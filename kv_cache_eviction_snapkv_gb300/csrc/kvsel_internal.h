@@ -40,7 +40,8 @@ struct ScoreArgs {
   float* part;             // [items][Wp][2] chunk (max, sum) in base-2 units
   int* counters;           // [instances] chunks that published their stats
   int* flags;              // [instances] 1 once the merged stats are written
-  float* final_stats;      // [instances][Wp] max + log2(sum) per window row
+  float* final_stats;      // [instances][Wp] max + log2(sum) per window row (CUDA-core
+                           // path); [instances][Wp][2] final (max, sum) slots (tensor cores)
   float* votes;            // [layers][H][T]
   float* logits;           // [layers][H][W][T] (logits mode only)
   int* status;             // device status word
