@@ -75,6 +75,7 @@ struct SelectArgs {
   int64_t max_prefix;      // largest L - W over the selected sequences
   int cluster;             // CTAs per instance (set by the launcher)
   int slice;               // prefix positions per CTA (set by the launcher)
+  int stage_bytes;         // shared bytes before the sort buffer (set by the launcher)
   int gather;              // 1: also copy the kept K/V rows (fused path)
   const void* k;           // gather: K, V and the compacted outputs
   const void* v;

@@ -351,27 +351,142 @@ __device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int6
   }
 }
 
-// One cluster of CS CTAs per (layer, sequence, head): CTA `rank` owns prefix
+// ---------------------------------------------------------------------------
+// Ascending sort of n = 512 * R u64 keys (R <= 8): every warp sorts its run of
+// 32R keys in registers and shuffles (bitonic, each lane holding R
+// consecutive keys), then rounds of merges double the sorted runs, each
+// thread placing R outputs found by a merge-path search. `tmp` (n keys) is
+// the ping-pong buffer; returns the buffer that holds the result. Every
+// thread of the block calls it.
+// ---------------------------------------------------------------------------
+
+template <int R>
+__device__ unsigned long long* sort_runs_merge(unsigned long long* buf, unsigned long long* tmp) {
+  constexpr int kRun = 32 * R;
+  constexpr int n = kSelThreads * R;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int base = warp * kRun + lane * R;   // this lane's keys
+  unsigned long long v[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) v[r] = buf[base + r];
+#pragma unroll
+  for (int size = 2; size <= kRun; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= R) {
+        const int lx = stride / R;  // partner lane distance
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], lx);
+          const int e = lane * R + r;  // index within the run
+          const bool up = size == kRun || (e & size) == 0;
+          const bool lower = (e & stride) == 0;
+          const unsigned long long mn = v[r] < o ? v[r] : o, mx = v[r] < o ? o : v[r];
+          v[r] = (lower == up) ? mn : mx;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if ((r & stride) == 0) {
+            const int e = lane * R + r;
+            const bool up = size == kRun || (e & size) == 0;
+            if ((v[r] > v[r | stride]) == up) {
+              const unsigned long long t = v[r];
+              v[r] = v[r | stride];
+              v[r | stride] = t;
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) buf[base + r] = v[r];
+  __syncthreads();
+  unsigned long long* src = buf;
+  unsigned long long* dst = tmp;
+  for (int len = kRun; len < n; len <<= 1) {
+    const int out0 = tid * R;
+    const int pbase = out0 / (2 * len) * (2 * len);
+    const unsigned long long* A = src + pbase;
+    const unsigned long long* B = A + len;
+    const int d = out0 - pbase;
+    // i = how many of the first d outputs come from A (keys are distinct
+    // except the padding, and A wins ties, which keeps the merge stable)
+    int lo = d > len ? d - len : 0, hi = d < len ? d : len;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (A[mid] <= B[d - mid - 1]) lo = mid + 1;
+      else hi = mid;
+    }
+    int i = lo, j = d - lo;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const bool take_a = j >= len || (i < len && A[i] <= B[j]);
+      dst[out0 + r] = take_a ? A[i] : B[j];
+      i += take_a;
+      j += !take_a;
+    }
+    __syncthreads();
+    unsigned long long* t = src;
+    src = dst;
+    dst = t;
+  }
+  return src;
+}
+
+// ---------------------------------------------------------------------------
+// The selection: one instance (layer, sequence, head) on a cluster of CS CTAs
+// (CS1: a single CTA, no distributed shared memory). CTA `rank` owns prefix
 // positions [rank * slice, (rank+1) * slice). Dynamic shared memory: stage |
 // sortbuf. `stage` holds the slice's votes with a zero halo of pool_k / 2 on
-// each side, and the slice's keys are written over it; the leader's
-// `sortbuf` receives every kept key of the cluster. With `a.gather` the
-// leader also copies the kept K/V rows (the fused path).
-template <int R>
-__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ SelShared sh;
+// each side; the slice's keys are written over it, and once they are emitted
+// it serves as the sort's second buffer. The leader's `sortbuf` receives
+// every kept key of the cluster. With `gather_here` the leader also copies
+// the kept K/V rows.
+// ---------------------------------------------------------------------------
+
+// Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
+// instance's C: reads their positions from the leader's sorted keys (`sort_r`,
+// its shared window) into `idx`, waits at a cluster barrier (after which the
+// leader's shared memory may go), then copies the rows.
+__device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs, uint32_t rank,
+                                  uint32_t sort_r, int32_t* idx, int64_t src_tok0,
+                                  int64_t out_row0, int h) {
+  const int per = (a.C + cs - 1) / cs;
+  const int s0 = min(a.C, (int)rank * per), s1 = min(a.C, s0 + per);
+  for (int s = s0 + (int)threadIdx.x; s < s1; s += kSelThreads) {
+    int32_t v;
+    if (s < (int)k) {
+      uint32_t lo;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(lo) : "r"(sort_r + 8u * s) : "memory");
+      v = (int32_t)lo;  // the position: low word of (~key << 32 | position)
+    } else {
+      v = P + (s - (int)k);
+    }
+    idx[s - s0] = v;
+  }
+  __syncthreads();
+  cluster_sync();
+  gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, [&](int s) { return (int)idx[s]; });
+}
+
+template <bool CS1>
+__device__ __forceinline__ void sel_sync() {
+  if constexpr (CS1) __syncthreads();
+  else cluster_sync();
+}
+
+template <int R, bool CS1>
+__device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
+                                unsigned char* smem, SelShared& sh, bool gather_here) {
   const int pad = a.pool_inline ? (a.pool_k >> 1) : 0;
   float* stage = reinterpret_cast<float*>(smem);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  unsigned long long* sortbuf = reinterpret_cast<unsigned long long*>(
-      smem + ((((size_t)a.slice + 2 * pad) * 4 + 15) & ~size_t(15)));
+  unsigned long long* sortbuf = reinterpret_cast<unsigned long long*>(smem + a.stage_bytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t rank = cluster_rank();
-  const int cs = a.cluster;
-  const int inst = blockIdx.x / cs;            // ((layer * S) + b) * H + h
-  const int h = inst % a.H;
+  const int h = inst % a.H;                    // inst = ((layer * S) + b) * H + h
   const int lb = inst / a.H;
   const int b = lb % a.n_seqs;
   const int layer = lb / a.n_seqs;
@@ -381,11 +496,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
   int32_t* out = a.out_idx + out_row0 * a.H + h;
   const int64_t src_tok0 = (int64_t)layer * a.T + sd.tok_off;
 
-  if (L < a.C) {  // bypass: keep everything in order (uniform over the cluster)
-    if (rank == 0) {
-      for (int s = tid; s < L; s += kSelThreads) out[(int64_t)s * a.H] = s;
-      if (a.gather) gather_any(a, L, src_tok0, out_row0, h, [](int s) { return s; });
-    }
+  const int cs = CS1 ? 1 : a.cluster;
+  if (L < a.C) {  // bypass: keep everything in order, each CTA a share of the rows
+    const int per = (L + cs - 1) / cs, s0 = min(L, (int)rank * per), s1 = min(L, s0 + per);
+    for (int s = s0 + tid; s < s1; s += kSelThreads) out[(int64_t)s * a.H] = s;
+    if (gather_here)
+      gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, [&](int s) { return s0 + s; });
     return;
   }
   const int P = L - a.W;
@@ -395,34 +511,44 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
   const int n = max(0, j1 - j0);
   const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sd.tok_off;
   const float* src = a.scores + plane;
+  // the cluster's histogram, result and counts live in the leader
+  uint32_t* ghist = CS1 ? sh.hist : sh.ghist;
+  const uint32_t ghist_r = CS1 ? 0u : dsmem_addr(sh.ghist, 0);
+  const uint32_t res_r = CS1 ? 0u : dsmem_addr(sh.res, 0);
+  const uint32_t cnt_r = CS1 ? 0u : dsmem_addr(sh.cnt, 0);
+  const uint32_t sort_r = CS1 ? 0u : dsmem_addr(sortbuf, 0);
 
-  const uint32_t ghist_r = dsmem_addr(sh.ghist, 0);
-  const uint32_t res_r = dsmem_addr(sh.res, 0);
-  const uint32_t cnt_r = dsmem_addr(sh.cnt, 0);
-  const uint32_t sort_r = dsmem_addr(sortbuf, 0);
-
-  // ---- keys: stage the scores (with the zero halo), then, chunk by chunk,
-  // read each position's window and write its key at stage index j - j0,
-  // which only overwrites votes no later window needs.
+  // ---- stage the scores with the zero halo; clear the first pass's histograms
   for (int c = tid; c < n + 2 * pad; c += kSelThreads) {
     const int j = j0 - pad + c;
     stage[c] = (j >= 0 && j < P) ? src[j] : 0.f;
   }
+  for (int i = tid; i < kBins; i += kSelThreads) {
+    sh.hist[i] = 0;
+    if (!CS1 && rank == 0) sh.ghist[i] = 0;
+  }
   __syncthreads();
-  for (int c0 = 0; c0 < n; c0 += kSelThreads) {
+  // ---- keys, chunk by chunk: read each position's window, count its key
+  // into the first pass's histogram (top 11 bits), and (after a barrier)
+  // write the key at stage index j - j0, which only overwrites votes no later
+  // window needs
+  for (int c0 = 0; c0 < n; c0 += kSelThreads) {  // uniform trips
     const int i = c0 + tid;
-    uint32_t key = 0u;
+    uint32_t key = 0u, bin = kNoBin;
     if (i < n) {
       const float v = a.pool_inline ? pool_any(stage, i + pad, a.pool_kind, a.pool_k) : stage[i];
       key = score_key(v, a.status);
+      bin = key >> 21;
     }
+    add_bin(sh.hist, bin, lane);
     __syncthreads();
     if (i < n) keys[i] = key;
   }
-  if (rank == 0)
-    for (int i = tid; i < kBins; i += kSelThreads) sh.ghist[i] = 0;
-  __syncthreads();
-  cluster_sync();
+  if constexpr (!CS1) {
+    for (int i = tid; i < kBins; i += kSelThreads)
+      if (sh.hist[i]) dsmem_add_u32(ghist_r + 4u * i, sh.hist[i]);
+  }
+  sel_sync<CS1>();
 
   // ---- three radix passes over (11, 11, 10) bits, summed in the leader
   uint32_t krem = k, prefix = 0;
@@ -431,26 +557,32 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
     const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
     const int nb = pass == 2 ? 1024 : kBins;
     const int hi_shift = pass == 0 ? 32 : pass == 1 ? 21 : 10;
-    for (int i = tid; i < nb; i += kSelThreads) sh.hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n_up; i += kSelThreads) {
-      uint32_t bin = kNoBin;
-      if (i < n) {
-        const uint32_t key = keys[i];
-        if (pass == 0 || (key >> hi_shift) == prefix) bin = (key >> shift) & (uint32_t)(nb - 1);
+    if (pass > 0) {
+      for (int i = tid; i < nb; i += kSelThreads) sh.hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < n_up; i += kSelThreads) {
+        uint32_t bin = kNoBin;
+        if (i < n) {
+          const uint32_t key = keys[i];
+          if ((key >> hi_shift) == prefix) bin = (key >> shift) & (uint32_t)(nb - 1);
+        }
+        add_bin(sh.hist, bin, lane);
       }
-      add_bin(sh.hist, bin, lane);
+      __syncthreads();
+      if constexpr (!CS1) {
+        for (int i = tid; i < nb; i += kSelThreads)
+          if (sh.hist[i]) dsmem_add_u32(ghist_r + 4u * i, sh.hist[i]);
+        cluster_sync();
+      }
     }
-    __syncthreads();
-    for (int i = tid; i < nb; i += kSelThreads)
-      if (sh.hist[i]) dsmem_add_u32(ghist_r + 4u * i, sh.hist[i]);
-    cluster_sync();
-    if (rank == 0) {
-      find_bin_block(sh.ghist, nb, krem, sh.res, sh.wsum);
-      for (int i = tid; i < nb; i += kSelThreads) sh.ghist[i] = 0;
+    if (CS1 || rank == 0) {
+      find_bin_block(ghist, nb, krem, sh.res, sh.wsum);
+      if constexpr (!CS1)
+        for (int i = tid; i < nb; i += kSelThreads) sh.ghist[i] = 0;
     }
-    cluster_sync();
-    const uint32_t d = dsmem_ld_u32(res_r), above = dsmem_ld_u32(res_r + 4);
+    sel_sync<CS1>();
+    const uint32_t d = CS1 ? sh.res[0] : dsmem_ld_u32(res_r);
+    const uint32_t above = CS1 ? sh.res[1] : dsmem_ld_u32(res_r + 4);
     prefix = (prefix << (pass == 2 ? 10 : 11)) | d;
     krem -= above;
   }
@@ -476,20 +608,25 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
     slice_gt += sh.warp_cnt[w][0];
     slice_eq += sh.warp_cnt[w][1];
   }
-  if (tid == 0) {
-    dsmem_st_u32(cnt_r + 8u * rank, slice_gt);
-    dsmem_st_u32(cnt_r + 8u * rank + 4u, slice_eq);
-  }
-  cluster_sync();
-  uint32_t eq_base = 0, sel_base = 0, take_eq = 0;
-  for (int r = 0; r <= (int)rank; ++r) {
-    const uint32_t g = dsmem_ld_u32(cnt_r + 8u * r), q = dsmem_ld_u32(cnt_r + 8u * r + 4u);
-    const uint32_t take = need_eq > eq_base ? min(q, need_eq - eq_base) : 0u;
-    if (r == (int)rank) {
-      take_eq = take;
-    } else {
-      sel_base += g + take;
-      eq_base += q;
+  uint32_t sel_base = 0, take_eq = 0;
+  if constexpr (CS1) {
+    take_eq = min(slice_eq, need_eq);
+  } else {
+    if (tid == 0) {
+      dsmem_st_u32(cnt_r + 8u * rank, slice_gt);
+      dsmem_st_u32(cnt_r + 8u * rank + 4u, slice_eq);
+    }
+    cluster_sync();
+    uint32_t eq_base = 0;
+    for (int r = 0; r <= (int)rank; ++r) {
+      const uint32_t g = dsmem_ld_u32(cnt_r + 8u * r), q = dsmem_ld_u32(cnt_r + 8u * r + 4u);
+      const uint32_t take = need_eq > eq_base ? min(q, need_eq - eq_base) : 0u;
+      if (r == (int)rank) {
+        take_eq = take;
+      } else {
+        sel_base += g + take;
+        eq_base += q;
+      }
     }
   }
   // equal keys of this slice to keep: the first take_eq in position order
@@ -541,12 +678,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
   pos += incl - mine;
   for (int i = tid; mask; i += kSelThreads) {
     if (mask & 1u) {
-      dsmem_st_u64(sort_r + 8u * pos, ((unsigned long long)(~keys[i]) << 32) | (uint32_t)(j0 + i));
+      const unsigned long long ck = ((unsigned long long)(~keys[i]) << 32) | (uint32_t)(j0 + i);
+      if constexpr (CS1) sortbuf[pos] = ck;
+      else dsmem_st_u64(sort_r + 8u * pos, ck);
       ++pos;
     }
     mask >>= 1;
   }
-  cluster_sync();
+  sel_sync<CS1>();
+  if (!CS1 && gather_here && rank != 0) {
+    // the leader sorts; then every CTA copies a share of the kept rows, its
+    // positions read from the leader's sorted keys
+    cluster_sync();
+    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), src_tok0,
+                      out_row0, h);
+    return;
+  }
   if (rank != 0) return;
 
   // ---- leader: sort (larger score first, then smaller position), write the
@@ -554,16 +701,37 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(SelectArgs a) {
   const int n2 = kSelThreads * R;
   for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
   __syncthreads();
-  bitonic_sort_blocked<R>(sortbuf, kSelThreads);
+  if constexpr (R <= 8) {
+    // the staged keys are no longer needed: the stage (sized by the launcher
+    // for at least n2 keys) is the merge buffer; an even number of merge
+    // rounds leaves the result in sortbuf
+    sort_runs_merge<R>(sortbuf, reinterpret_cast<unsigned long long*>(smem));
+  } else {
+    bitonic_sort_blocked<R>(sortbuf, kSelThreads);
+  }
   for (int s = tid; s < (int)k; s += kSelThreads)
     out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
   for (int w = tid; w < a.W; w += kSelThreads) out[(int64_t)(k + w) * a.H] = P + w;
-  if (a.gather) {
+  if (!gather_here) return;
+  if (CS1) {
     const int kk = (int)k;
     gather_any(a, a.C, src_tok0, out_row0, h, [&](int s) {
       return s < kk ? (int)(sortbuf[s] & 0xFFFFFFFFull) : P + (s - kk);
     });
+  } else {
+    __syncthreads();
+    cluster_sync();
+    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), src_tok0,
+                      out_row0, h);
   }
+}
+
+template <int R, bool CS1>
+__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const __grid_constant__ SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ SelShared sh;
+  select_instance<R, CS1>(a, blockIdx.x / a.cluster, CS1 ? 0u : cluster_rank(), smem, sh,
+                          a.gather != 0);
 }
 
 }  // namespace
@@ -591,18 +759,24 @@ cudaError_t launch_select(const SelectArgs& a0) {
   int n2 = kSelThreads;
   while (n2 < a.C - a.W) n2 <<= 1;
   const int pad = a.pool_inline ? a.pool_k / 2 : 0;
-  const size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
+  size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
+  if (n2 <= kSelThreads * 8) stage = std::max(stage, (size_t)n2 * 8);  // the merge buffer
+  stage = std::max(stage, (size_t)((a.C + cs - 1) / cs) * 4);           // a CTA's copy share
+  a.stage_bytes = (int)stage;
   const size_t smem = stage + (size_t)n2 * 8;
-  void (*kern)(SelectArgs) = nullptr;
+  void (*kern)(const SelectArgs) = nullptr;
+#define KVSEL_SEL_CASE(RR) \
+  case RR: kern = cs == 1 ? select_kernel<RR, true> : select_kernel<RR, false>; break;
   switch (n2 / kSelThreads) {
-    case 1: kern = select_kernel<1>; break;
-    case 2: kern = select_kernel<2>; break;
-    case 4: kern = select_kernel<4>; break;
-    case 8: kern = select_kernel<8>; break;
-    case 16: kern = select_kernel<16>; break;
-    case 32: kern = select_kernel<32>; break;
+    KVSEL_SEL_CASE(1)
+    KVSEL_SEL_CASE(2)
+    KVSEL_SEL_CASE(4)
+    KVSEL_SEL_CASE(8)
+    KVSEL_SEL_CASE(16)
+    KVSEL_SEL_CASE(32)
     default: return cudaErrorInvalidValue;
   }
+#undef KVSEL_SEL_CASE
   if (a.gather) {
     auto ok = [&](int vw) {
       if (a.row_bytes % vw) return false;
@@ -612,8 +786,9 @@ cudaError_t launch_select(const SelectArgs& a0) {
     };
     a.vec_bytes = ok(16) ? 16 : ok(8) ? 8 : ok(4) ? 4 : 2;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e) return e;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(blocks * cs));
   cfg.blockDim = dim3(kSelThreads);
