@@ -27,6 +27,7 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMaxCluster = 8;   // portable cluster size
+constexpr int kSelSmemMax = 227 * 1024;  // opt-in shared memory per CTA
 
 // Order-keeping key: larger float -> larger key; -0 == +0; NaN lowest.
 __device__ __forceinline__ uint32_t score_key(float v, int* status) {
@@ -352,56 +353,59 @@ __device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int6
 }
 
 // ---------------------------------------------------------------------------
-// Ascending sort of n = 512 * R u64 keys (R <= 8): every warp sorts its run of
-// 32R keys in registers and shuffles (bitonic, each lane holding R
+// Ascending sort of n = 512 * R u64 keys in `buf`: runs of 128 keys are
+// sorted by the warps in registers and shuffles (bitonic, each lane holding 4
 // consecutive keys), then rounds of merges double the sorted runs, each
-// thread placing R outputs found by a merge-path search. `tmp` (n keys) is
-// the ping-pong buffer; returns the buffer that holds the result. Every
-// thread of the block calls it.
+// thread placing R consecutive outputs found by a merge-path search. `tmp`
+// (n keys) is the ping-pong buffer; the result ends in `buf`. Every thread
+// of the block calls it.
 // ---------------------------------------------------------------------------
 
 template <int R>
-__device__ unsigned long long* sort_runs_merge(unsigned long long* buf, unsigned long long* tmp) {
-  constexpr int kRun = 32 * R;
+__device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp) {
+  constexpr int kPer = 4;                  // keys per lane in the run sort
+  constexpr int kRun = 32 * kPer;
   constexpr int n = kSelThreads * R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int base = warp * kRun + lane * R;   // this lane's keys
-  unsigned long long v[R];
+  for (int run = warp; run < n / kRun; run += kSelWarps) {
+    const int base = run * kRun + lane * kPer;
+    unsigned long long v[kPer];
 #pragma unroll
-  for (int r = 0; r < R; ++r) v[r] = buf[base + r];
+    for (int r = 0; r < kPer; ++r) v[r] = buf[base + r];
 #pragma unroll
-  for (int size = 2; size <= kRun; size <<= 1) {
+    for (int size = 2; size <= kRun; size <<= 1) {
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= R) {
-        const int lx = stride / R;  // partner lane distance
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        if (stride >= kPer) {
+          const int lx = stride / kPer;  // partner lane distance
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], lx);
-          const int e = lane * R + r;  // index within the run
-          const bool up = size == kRun || (e & size) == 0;
-          const bool lower = (e & stride) == 0;
-          const unsigned long long mn = v[r] < o ? v[r] : o, mx = v[r] < o ? o : v[r];
-          v[r] = (lower == up) ? mn : mx;
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if ((r & stride) == 0) {
-            const int e = lane * R + r;
+          for (int r = 0; r < kPer; ++r) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], lx);
+            const int e = lane * kPer + r;  // index within the run
             const bool up = size == kRun || (e & size) == 0;
-            if ((v[r] > v[r | stride]) == up) {
-              const unsigned long long t = v[r];
-              v[r] = v[r | stride];
-              v[r | stride] = t;
+            const bool lower = (e & stride) == 0;
+            const unsigned long long mn = v[r] < o ? v[r] : o, mx = v[r] < o ? o : v[r];
+            v[r] = (lower == up) ? mn : mx;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kPer; ++r) {
+            if ((r & stride) == 0) {
+              const int e = lane * kPer + r;
+              const bool up = size == kRun || (e & size) == 0;
+              if ((v[r] > v[r | stride]) == up) {
+                const unsigned long long t = v[r];
+                v[r] = v[r | stride];
+                v[r | stride] = t;
+              }
             }
           }
         }
       }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) buf[base + r] = v[r];
+    for (int r = 0; r < kPer; ++r) buf[base + r] = v[r];
+  }
   __syncthreads();
   unsigned long long* src = buf;
   unsigned long long* dst = tmp;
@@ -420,7 +424,7 @@ __device__ unsigned long long* sort_runs_merge(unsigned long long* buf, unsigned
       else hi = mid;
     }
     int i = lo, j = d - lo;
-#pragma unroll
+#pragma unroll 4
     for (int r = 0; r < R; ++r) {
       const bool take_a = j >= len || (i < len && A[i] <= B[j]);
       dst[out0 + r] = take_a ? A[i] : B[j];
@@ -432,19 +436,11 @@ __device__ unsigned long long* sort_runs_merge(unsigned long long* buf, unsigned
     src = dst;
     dst = t;
   }
-  return src;
+  if (src != buf) {  // an odd number of rounds
+    for (int e = tid; e < n; e += kSelThreads) buf[e] = src[e];
+    __syncthreads();
+  }
 }
-
-// ---------------------------------------------------------------------------
-// The selection: one instance (layer, sequence, head) on a cluster of CS CTAs
-// (CS1: a single CTA, no distributed shared memory). CTA `rank` owns prefix
-// positions [rank * slice, (rank+1) * slice). Dynamic shared memory: stage |
-// sortbuf. `stage` holds the slice's votes with a zero halo of pool_k / 2 on
-// each side; the slice's keys are written over it, and once they are emitted
-// it serves as the sort's second buffer. The leader's `sortbuf` receives
-// every kept key of the cluster. With `gather_here` the leader also copies
-// the kept K/V rows.
-// ---------------------------------------------------------------------------
 
 // Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
 // instance's C: reads their positions from the leader's sorted keys (`sort_r`,
@@ -701,10 +697,8 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const int n2 = kSelThreads * R;
   for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
   __syncthreads();
-  if constexpr (R <= 8) {
-    // the staged keys are no longer needed: the stage (sized by the launcher
-    // for at least n2 keys) is the merge buffer; an even number of merge
-    // rounds leaves the result in sortbuf
+  if (a.stage_bytes >= n2 * 8) {
+    // the staged keys are no longer needed: the stage is the merge buffer
     sort_runs_merge<R>(sortbuf, reinterpret_cast<unsigned long long*>(smem));
   } else {
     bitonic_sort_blocked<R>(sortbuf, kSelThreads);
@@ -760,7 +754,8 @@ cudaError_t launch_select(const SelectArgs& a0) {
   while (n2 < a.C - a.W) n2 <<= 1;
   const int pad = a.pool_inline ? a.pool_k / 2 : 0;
   size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
-  if (n2 <= kSelThreads * 8) stage = std::max(stage, (size_t)n2 * 8);  // the merge buffer
+  // the merge sort's second buffer, where the shared memory allows it
+  if ((size_t)n2 * 8 * 2 + 4096 <= (size_t)kSelSmemMax) stage = std::max(stage, (size_t)n2 * 8);
   stage = std::max(stage, (size_t)((a.C + cs - 1) / cs) * 4);           // a CTA's copy share
   a.stage_bytes = (int)stage;
   const size_t smem = stage + (size_t)n2 * 8;
