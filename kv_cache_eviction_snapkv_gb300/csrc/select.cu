@@ -27,7 +27,6 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMaxCluster = 8;   // portable cluster size
-constexpr int kSelSmemMax = 227 * 1024;  // opt-in shared memory per CTA
 
 // Order-keeping key: larger float -> larger key; -0 == +0; NaN lowest.
 __device__ __forceinline__ uint32_t score_key(float v, int* status) {
@@ -249,7 +248,6 @@ __device__ void bitonic_sort_blocked(unsigned long long* buf, int nt) {
 
 struct SelShared {
   uint32_t hist[kBins];        // this CTA's histogram
-  uint32_t ghist[kBins];       // leader: the cluster's histogram
   uint32_t res[2];             // leader: (bin, count above)
   uint32_t cnt[kMaxCluster][2];  // leader: per rank (greater, equal) counts
   uint32_t warp_cnt[kSelWarps][2];
@@ -356,10 +354,14 @@ __device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int6
 // Ascending sort of n = 512 * R u64 keys in `buf`: runs of 128 keys are
 // sorted by the warps in registers and shuffles (bitonic, each lane holding 4
 // consecutive keys), then rounds of merges double the sorted runs, each
-// thread placing R consecutive outputs found by a merge-path search. `tmp`
-// (n keys) is the ping-pong buffer; the result ends in `buf`. Every thread
-// of the block calls it.
+// thread placing R consecutive outputs found by a merge-path search. During
+// the merges key e sits at e + e / 16 (one 8-byte gap per 128 bytes), so the
+// lanes' R-strided accesses spread over the banks. `tmp` and `buf` both hold
+// n * 17 / 16 keys; the result ends in `buf`, unskewed. Every thread of the
+// block calls it.
 // ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int skw(int e) { return e + (e >> 4); }
 
 template <int R>
 __device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp) {
@@ -404,30 +406,30 @@ __device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp
       }
     }
 #pragma unroll
-    for (int r = 0; r < kPer; ++r) buf[base + r] = v[r];
+    for (int r = 0; r < kPer; ++r) tmp[skw(base + r)] = v[r];
   }
   __syncthreads();
-  unsigned long long* src = buf;
-  unsigned long long* dst = tmp;
+  unsigned long long* src = tmp;
+  unsigned long long* dst = buf;
   for (int len = kRun; len < n; len <<= 1) {
     const int out0 = tid * R;
     const int pbase = out0 / (2 * len) * (2 * len);
-    const unsigned long long* A = src + pbase;
-    const unsigned long long* B = A + len;
     const int d = out0 - pbase;
-    // i = how many of the first d outputs come from A (keys are distinct
-    // except the padding, and A wins ties, which keeps the merge stable)
+    // i = how many of the first d outputs come from A = [pbase, pbase + len)
+    // (keys are distinct except the padding, and A wins ties: a stable merge)
     int lo = d > len ? d - len : 0, hi = d < len ? d : len;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (A[mid] <= B[d - mid - 1]) lo = mid + 1;
+      if (src[skw(pbase + mid)] <= src[skw(pbase + len + d - mid - 1)]) lo = mid + 1;
       else hi = mid;
     }
     int i = lo, j = d - lo;
 #pragma unroll 4
     for (int r = 0; r < R; ++r) {
-      const bool take_a = j >= len || (i < len && A[i] <= B[j]);
-      dst[out0 + r] = take_a ? A[i] : B[j];
+      const unsigned long long x = i < len ? src[skw(pbase + i)] : ~0ull;
+      const unsigned long long y = j < len ? src[skw(pbase + len + j)] : ~0ull;
+      const bool take_a = j >= len || (i < len && x <= y);
+      dst[skw(out0 + r)] = take_a ? x : y;
       i += take_a;
       j += !take_a;
     }
@@ -436,10 +438,14 @@ __device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp
     src = dst;
     dst = t;
   }
-  if (src != buf) {  // an odd number of rounds
-    for (int e = tid; e < n; e += kSelThreads) buf[e] = src[e];
-    __syncthreads();
-  }
+  // unskew into buf (through registers when the result is in buf itself)
+  unsigned long long v[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) v[r] = src[skw(tid + r * kSelThreads)];
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) buf[tid + r * kSelThreads] = v[r];
+  __syncthreads();
 }
 
 // Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
@@ -508,8 +514,10 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sd.tok_off;
   const float* src = a.scores + plane;
   // the cluster's histogram, result and counts live in the leader
-  uint32_t* ghist = CS1 ? sh.hist : sh.ghist;
-  const uint32_t ghist_r = CS1 ? 0u : dsmem_addr(sh.ghist, 0);
+  // the leader's cluster histogram lives in its sort buffer, unused until
+  // the kept keys are emitted (the launcher gives it at least kBins words)
+  uint32_t* ghist = CS1 ? sh.hist : reinterpret_cast<uint32_t*>(sortbuf);
+  const uint32_t ghist_r = CS1 ? 0u : dsmem_addr(ghist, 0);
   const uint32_t res_r = CS1 ? 0u : dsmem_addr(sh.res, 0);
   const uint32_t cnt_r = CS1 ? 0u : dsmem_addr(sh.cnt, 0);
   const uint32_t sort_r = CS1 ? 0u : dsmem_addr(sortbuf, 0);
@@ -521,7 +529,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   }
   for (int i = tid; i < kBins; i += kSelThreads) {
     sh.hist[i] = 0;
-    if (!CS1 && rank == 0) sh.ghist[i] = 0;
+    if (!CS1 && rank == 0) ghist[i] = 0;
   }
   __syncthreads();
   // ---- keys, chunk by chunk: read each position's window, count its key
@@ -574,7 +582,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     if (CS1 || rank == 0) {
       find_bin_block(ghist, nb, krem, sh.res, sh.wsum);
       if constexpr (!CS1)
-        for (int i = tid; i < nb; i += kSelThreads) sh.ghist[i] = 0;
+        for (int i = tid; i < nb; i += kSelThreads) ghist[i] = 0;
     }
     sel_sync<CS1>();
     const uint32_t d = CS1 ? sh.res[0] : dsmem_ld_u32(res_r);
@@ -697,8 +705,9 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const int n2 = kSelThreads * R;
   for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
   __syncthreads();
-  if (a.stage_bytes >= n2 * 8) {
-    // the staged keys are no longer needed: the stage is the merge buffer
+  if constexpr (R <= 16) {
+    // the staged keys are no longer needed: the stage (sized by the launcher)
+    // is the merge buffer
     sort_runs_merge<R>(sortbuf, reinterpret_cast<unsigned long long*>(smem));
   } else {
     bitonic_sort_blocked<R>(sortbuf, kSelThreads);
@@ -754,11 +763,14 @@ cudaError_t launch_select(const SelectArgs& a0) {
   while (n2 < a.C - a.W) n2 <<= 1;
   const int pad = a.pool_inline ? a.pool_k / 2 : 0;
   size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
-  // the merge sort's second buffer, where the shared memory allows it
-  if ((size_t)n2 * 8 * 2 + 4096 <= (size_t)kSelSmemMax) stage = std::max(stage, (size_t)n2 * 8);
+  // the merge sort (R <= 16) skews its two buffers by 1/16
+  const size_t merge_bytes = (size_t)n2 * 17 / 16 * 8;
+  const bool merge = n2 <= kSelThreads * 16;
+  if (merge) stage = std::max(stage, merge_bytes);
   stage = std::max(stage, (size_t)((a.C + cs - 1) / cs) * 4);           // a CTA's copy share
   a.stage_bytes = (int)stage;
-  const size_t smem = stage + (size_t)n2 * 8;
+  const size_t sortbuf = std::max(merge ? merge_bytes : (size_t)n2 * 8, (size_t)kBins * 4);
+  const size_t smem = stage + sortbuf;
   void (*kern)(const SelectArgs) = nullptr;
 #define KVSEL_SEL_CASE(RR) \
   case RR: kern = cs == 1 ? select_kernel<RR, true> : select_kernel<RR, false>; break;
