@@ -448,6 +448,54 @@ __device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp
   __syncthreads();
 }
 
+// Key pass for pooling width K <= 9: each thread pools four consecutive
+// positions per round (2048 per round, one barrier each), reading their
+// windows as aligned float4s from the zero-padded stage (vote of slice
+// position i at stage[i + K/2]; the stage has 16 floats of slack past its end).
+// Sums and maxima run in increasing position order, as in pool_fixed. Keys go
+// to keys[i] = stage[i] after the round's barrier, counted into `hist` by
+// their top 11 bits.
+template <int K>
+__device__ void key_pass4(float* stage, int n, int kind, uint32_t* hist, int* status) {
+  constexpr int kW = (K + 3 + 3) / 4;  // float4s covering positions i0 .. i0+3's windows
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(stage);
+  for (int c0 = 0; c0 < n; c0 += 4 * kSelThreads) {  // uniform trips
+    const int i0 = c0 + 4 * tid;
+    float w[4 * kW];
+#pragma unroll
+    for (int q = 0; q < kW; ++q) {
+      const float4 f = i0 < n ? *reinterpret_cast<const float4*>(stage + i0 + 4 * q)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[4 * q] = f.x;
+      w[4 * q + 1] = f.y;
+      w[4 * q + 2] = f.z;
+      w[4 * q + 3] = f.w;
+    }
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float v;
+      if (kind == KVSEL_POOL_AVG) {
+        float acc = 0.f;
+#pragma unroll
+        for (int d = 0; d < K; ++d) acc += w[u + d];
+        v = acc / (float)K;
+      } else {
+        v = w[u];
+#pragma unroll
+        for (int d = 1; d < K; ++d) v = fmaxf(v, w[u + d]);
+      }
+      key[u] = i0 + u < n ? score_key(v, status) : 0u;
+      add_bin(hist, i0 + u < n ? key[u] >> 21 : kNoBin, lane);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u < n) keys[i0 + u] = key[u];
+  }
+}
+
 // Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
 // instance's C: reads their positions from the leader's sorted keys (`sort_r`,
 // its shared window) into `idx`, waits at a cluster barrier (after which the
@@ -532,21 +580,30 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     if (!CS1 && rank == 0) ghist[i] = 0;
   }
   __syncthreads();
-  // ---- keys, chunk by chunk: read each position's window, count its key
-  // into the first pass's histogram (top 11 bits), and (after a barrier)
-  // write the key at stage index j - j0, which only overwrites votes no later
-  // window needs
-  for (int c0 = 0; c0 < n; c0 += kSelThreads) {  // uniform trips
-    const int i = c0 + tid;
-    uint32_t key = 0u, bin = kNoBin;
-    if (i < n) {
-      const float v = a.pool_inline ? pool_any(stage, i + pad, a.pool_kind, a.pool_k) : stage[i];
-      key = score_key(v, a.status);
-      bin = key >> 21;
+  // ---- keys, counted into the first pass's histogram (top 11 bits) and
+  // written at stage index j - j0, over votes no later window needs
+  if (a.pool_inline && a.pool_k <= 9) {
+    switch (a.pool_k) {
+      case 1: key_pass4<1>(stage, n, a.pool_kind, sh.hist, a.status); break;
+      case 3: key_pass4<3>(stage, n, a.pool_kind, sh.hist, a.status); break;
+      case 5: key_pass4<5>(stage, n, a.pool_kind, sh.hist, a.status); break;
+      case 7: key_pass4<7>(stage, n, a.pool_kind, sh.hist, a.status); break;
+      default: key_pass4<9>(stage, n, a.pool_kind, sh.hist, a.status); break;
     }
-    add_bin(sh.hist, bin, lane);
-    __syncthreads();
-    if (i < n) keys[i] = key;
+  } else {
+    // one position per thread and chunk (any width, or no pooling)
+    for (int c0 = 0; c0 < n; c0 += kSelThreads) {  // uniform trips
+      const int i = c0 + tid;
+      uint32_t key = 0u, bin = kNoBin;
+      if (i < n) {
+        const float v = a.pool_inline ? pool_any(stage, i + pad, a.pool_kind, a.pool_k) : stage[i];
+        key = score_key(v, a.status);
+        bin = key >> 21;
+      }
+      add_bin(sh.hist, bin, lane);
+      __syncthreads();
+      if (i < n) keys[i] = key;
+    }
   }
   if constexpr (!CS1) {
     for (int i = tid; i < kBins; i += kSelThreads)
@@ -762,7 +819,8 @@ cudaError_t launch_select(const SelectArgs& a0) {
   int n2 = kSelThreads;
   while (n2 < a.C - a.W) n2 <<= 1;
   const int pad = a.pool_inline ? a.pool_k / 2 : 0;
-  size_t stage = ((((size_t)a.slice + 2 * pad) * 4) + 15) & ~size_t(15);
+  // (16 floats of slack: the four-wide key pass reads whole float4s)
+  size_t stage = ((((size_t)a.slice + 2 * pad + 16) * 4) + 15) & ~size_t(15);
   // the merge sort (R <= 16) skews its two buffers by 1/16
   const size_t merge_bytes = (size_t)n2 * 17 / 16 * 8;
   const bool merge = n2 <= kSelThreads * 16;
