@@ -18,3 +18,4 @@ from .snapkv_oracle import (  # noqa: F401
     window_logits,
     window_row_exp_sums,
 )
+from .gqa_oracle import snapkv_group, snapkv_packed_gqa  # noqa: F401,E402
