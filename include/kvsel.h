@@ -84,14 +84,20 @@ enum { KVSEL_BF16 = 0, KVSEL_F32 = 1 };
 /* Shape of one call. num_layers >= 1 and num_heads >= 1 and head_dim >= 1;
  * num_seqs >= 0 (0 = nothing to do); dtype is KVSEL_BF16 or KVSEL_F32 (for
  * q_win, K, V and the gathered outputs). seq_offsets: HOST array of
- * num_seqs + 1 entries, seq_offsets[0] == 0, nondecreasing. */
+ * num_seqs + 1 entries, seq_offsets[0] == 0, nondecreasing.
+ * Grouped-query attention (page section "GQA 下的缓存节省不能只算 C 除以 L"):
+ * num_heads counts the query heads H (q_win and every per-head output) and
+ * num_kv_heads the heads H_kv of K and V: 0 (= num_heads) or a divisor of
+ * num_heads (else INVALID_ARG). Query head h then reads K/V head
+ * h / (H / H_kv), the expanded (repeat_kv) reading the page describes; the
+ * group-shared selection is kvsel_snapkv_grouped. */
 typedef struct kvsel_shape {
   int32_t num_layers;
   int32_t num_seqs;
   int32_t num_heads;
   int32_t head_dim;
   int32_t dtype;
-  int32_t reserved; /* must be 0 */
+  int32_t num_kv_heads; /* 0 = num_heads */
   const int64_t* seq_offsets;
 } kvsel_shape;
 
@@ -173,6 +179,21 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
                           const void* V, int32_t W, int32_t C, int32_t pool_kind,
                           int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
                           void* stream);
+
+/* Group-shared selection under grouped-query attention: one selection per
+ * (layer, sequence, K/V head), shared by the G = H / H_kv query heads of the
+ * group, so the kept cache has H_kv heads (the page leaves this design open;
+ * our reading): each query head computes its own causal-softmax votes against
+ * the group's keys, the group's vote of a prefix position is the sum of its
+ * G heads' votes (in head order), and pooling, the top-(C - W) selection and
+ * the gather then run once per group. Layouts: q_win [num_layers][S * W][H][D],
+ * K and V [num_layers][T][H_kv][D]; out_idx [num_layers][T_out][H_kv] int32,
+ * out_K and out_V [num_layers][T_out][H_kv][D]. Rules and limits those of
+ * kvsel_snapkv. With H_kv == H it is kvsel_snapkv. */
+kvsel_status kvsel_snapkv_grouped(const kvsel_shape* shape, const void* q_win, const void* K,
+                                  const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                                  int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                                  void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: the first device-side error recorded since the last call, or

@@ -16,7 +16,7 @@ c_i32, c_i64, c_u64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, cty
 class KvselShape(ctypes.Structure):
     """Mirror of ``kvsel_shape``."""
     _fields_ = [("num_layers", c_i32), ("num_seqs", c_i32), ("num_heads", c_i32),
-                ("head_dim", c_i32), ("dtype", c_i32), ("reserved", c_i32),
+                ("head_dim", c_i32), ("dtype", c_i32), ("num_kv_heads", c_i32),
                 ("seq_offsets", ctypes.POINTER(c_i64))]
 
 
@@ -34,6 +34,8 @@ SIGNATURES = {
     "kvsel_compact": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "kvsel_snapkv": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
                              c_vp, c_vp]),
+    "kvsel_snapkv_grouped": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
+                                     c_vp, c_vp, c_vp]),
     "kvsel_device_status": (c_i32, [c_vp]),
     "kvsel_set_wait_limit_ns": (c_i32, [c_u64]),
     "kvsel_debug_inject": (c_i32, [c_i32]),

@@ -61,11 +61,12 @@ class Shape:
     """Builds a ``kvsel_shape`` and keeps its host offsets alive."""
 
     def __init__(self, num_layers: int, num_heads: int, head_dim: int, dtype: int,
-                 seq_offsets: Sequence[int]):
+                 seq_offsets: Sequence[int], num_kv_heads: int = 0):
         offs = [int(x) for x in seq_offsets]
         self._offs = (ctypes.c_int64 * max(1, len(offs)))(*offs)
+        kv = 0 if int(num_kv_heads) == int(num_heads) else int(num_kv_heads)
         self.c = _native.KvselShape(int(num_layers), len(offs) - 1, int(num_heads),
-                                    int(head_dim), int(dtype), 0,
+                                    int(head_dim), int(dtype), kv,
                                     ctypes.cast(self._offs, ctypes.POINTER(ctypes.c_int64)))
         self.T = offs[-1] if offs else 0
 
@@ -99,11 +100,16 @@ def _need(t: torch.Tensor, name: str, dtype=None) -> None:
         raise ValueError(f"{name} must be {dtype}")
 
 
-def shape_of(K: torch.Tensor, seq_offsets: Sequence[int]) -> Shape:
+def shape_of(K: torch.Tensor, seq_offsets: Sequence[int], num_heads: Optional[int] = None
+             ) -> Shape:
+    """Shape of a call on K [layers, T, H_kv, D]; num_heads = the query (and
+    per-head output) heads, default H_kv (no grouped-query attention)."""
     K4 = _as4(K)
     if K4.dtype not in _DTYPES:
         raise ValueError("K must be bf16 or fp32")
-    return Shape(K4.shape[0], K4.shape[2], K4.shape[3], _DTYPES[K4.dtype], seq_offsets)
+    h = K4.shape[2] if num_heads is None else int(num_heads)
+    return Shape(K4.shape[0], h, K4.shape[3], _DTYPES[K4.dtype], seq_offsets,
+                 num_kv_heads=K4.shape[2])
 
 
 def kvsel_out_tokens(shape: Shape, C: int) -> int:
@@ -116,10 +122,10 @@ def kvsel_score_path(shape: Shape, W: int, C: int = 0) -> int:
 
 def kvsel_window_logits(q_win, K, seq_offsets, W: int, logits=None, stream=None):
     """Raw window logits [layers, H, W, T] fp32 (diagnostic)."""
-    sh = shape_of(K, seq_offsets)
     K4, q4 = _as4(K), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
     _need(K4, "K"), _need(q4, "q_win", K4.dtype)
-    L, _, H, _ = K4.shape
+    L, H = K4.shape[0], q4.shape[2]
     if logits is None:
         logits = torch.empty((L, H, int(W), sh.T), dtype=torch.float32, device=K.device)
     _need(logits, "logits", torch.float32)
@@ -131,10 +137,10 @@ def kvsel_window_logits(q_win, K, seq_offsets, W: int, logits=None, stream=None)
 def kvsel_score(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: int,
                 votes=None, pooled=None, want_votes: bool = True, stream=None):
     """(votes, pooled), each [layers, H, T] fp32; votes is None if not wanted."""
-    sh = shape_of(K, seq_offsets)
     K4, q4 = _as4(K), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
     _need(K4, "K"), _need(q4, "q_win", K4.dtype)
-    L, _, H, _ = K4.shape
+    L, H = K4.shape[0], q4.shape[2]
     if votes is None and want_votes:
         votes = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
     if pooled is None:
@@ -153,10 +159,10 @@ def kvsel_score_static(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: in
     """kvsel_score that allocates no device memory inside the library (its
     scratch is a fixed array in the library image); the output tensors are
     still the caller's."""
-    sh = shape_of(K, seq_offsets)
     K4, q4 = _as4(K), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
     _need(K4, "K"), _need(q4, "q_win", K4.dtype)
-    L, _, H, _ = K4.shape
+    L, H = K4.shape[0], q4.shape[2]
     if votes is None:
         votes = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
     if pooled is None:
@@ -187,11 +193,13 @@ def kvsel_select(pooled, seq_offsets, num_heads: int, W: int, C: int, out_idx=No
 
 
 def kvsel_compact(K, V, seq_offsets, out_idx, C: int, out_K=None, out_V=None, stream=None):
-    """(out_K, out_V) [layers, T_out, H, D] gathered with out_idx."""
-    sh = shape_of(K, seq_offsets)
+    """(out_K, out_V) [layers, T_out, H, D] gathered with out_idx [layers, T_out, H]
+    (H may be a multiple of K's heads: output head h reads K/V head h / (H / H_kv))."""
     K4, V4 = _as4(K), _as4(V)
+    H = out_idx.shape[-1]
+    sh = shape_of(K, seq_offsets, H)
     _need(K4, "K"), _need(V4, "V", K4.dtype), _need(out_idx, "out_idx", torch.int32)
-    L, _, H, D = K4.shape
+    L, D = K4.shape[0], K4.shape[3]
     t_out = kvsel_out_tokens(sh, C)
     if t_out < 0:
         raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_compact")
@@ -209,11 +217,12 @@ def kvsel_compact(K, V, seq_offsets, out_idx, C: int, out_K=None, out_V=None, st
 def kvsel_snapkv(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int, pool_k: int,
                  out_idx=None, out_K=None, out_V=None, stream=None
                  ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """The fused path: (out_idx, out_K, out_V)."""
-    sh = shape_of(K, seq_offsets)
+    """The fused path: (out_idx, out_K, out_V), over q_win's heads (with fewer
+    K/V heads, query head h reads K/V head h / (H / H_kv): the expanded reading)."""
     K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
     _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q_win", K4.dtype)
-    L, _, H, D = K4.shape
+    L, H, D = K4.shape[0], q4.shape[2], K4.shape[3]
     t_out = kvsel_out_tokens(sh, C)
     if t_out < 0:
         raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_snapkv")
@@ -229,6 +238,34 @@ def kvsel_snapkv(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int, pool_
     _check(_native.lib().kvsel_snapkv(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W), int(C),
                                       int(pool_kind), int(pool_k), _ptr(out_idx), _ptr(out_K),
                                       _ptr(out_V), _stream(stream)), "kvsel_snapkv")
+    return out_idx, out_K, out_V
+
+
+def kvsel_snapkv_grouped(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int,
+                         pool_k: int, out_idx=None, out_K=None, out_V=None, stream=None
+                         ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Group-shared selection (one per K/V head, votes of its query heads summed):
+    (out_idx [layers, T_out, H_kv], out_K, out_V [layers, T_out, H_kv, D])."""
+    K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q_win", K4.dtype)
+    L, Hkv, D = K4.shape[0], K4.shape[2], K4.shape[3]
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_snapkv_grouped")
+    dev = K.device
+    if out_idx is None:
+        out_idx = torch.empty((L, t_out, Hkv), dtype=torch.int32, device=dev)
+    if out_K is None:
+        out_K = torch.empty((L, t_out, Hkv, D), dtype=K.dtype, device=dev)
+    if out_V is None:
+        out_V = torch.empty((L, t_out, Hkv, D), dtype=K.dtype, device=dev)
+    _need(out_idx, "out_idx", torch.int32)
+    _need(out_K, "out_K", K4.dtype), _need(out_V, "out_V", K4.dtype)
+    _check(_native.lib().kvsel_snapkv_grouped(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W),
+                                              int(C), int(pool_kind), int(pool_k),
+                                              _ptr(out_idx), _ptr(out_K), _ptr(out_V),
+                                              _stream(stream)), "kvsel_snapkv_grouped")
     return out_idx, out_K, out_V
 
 

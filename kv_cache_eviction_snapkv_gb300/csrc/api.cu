@@ -122,6 +122,7 @@ struct Carve {
 
 struct Plan {
   int layers = 0, S = 0, H = 0, D = 0, dtype = 0;
+  int Hkv = 0, G = 1;             // K/V heads, query heads per K/V head
   int64_t T = 0, T_out = 0;
   int elem_bytes = 0;
   std::vector<SeqDesc> all;      // every sequence
@@ -130,14 +131,17 @@ struct Plan {
 
 kvsel_status plan_shape(const kvsel_shape* sh, int C, Plan* p) {
   if (!sh) return KVSEL_ERR_INVALID_ARG;
-  if (sh->num_layers < 1 || sh->num_seqs < 0 || sh->num_heads < 1 || sh->head_dim < 1 ||
-      sh->reserved != 0)
+  if (sh->num_layers < 1 || sh->num_seqs < 0 || sh->num_heads < 1 || sh->head_dim < 1)
     return KVSEL_ERR_INVALID_ARG;
+  const int hkv = sh->num_kv_heads == 0 ? sh->num_heads : sh->num_kv_heads;
+  if (hkv < 1 || sh->num_heads % hkv != 0) return KVSEL_ERR_INVALID_ARG;
   if (sh->dtype != KVSEL_BF16 && sh->dtype != KVSEL_F32) return KVSEL_ERR_INVALID_ARG;
   if (sh->num_seqs > 0 && !sh->seq_offsets) return KVSEL_ERR_INVALID_ARG;
   p->layers = sh->num_layers;
   p->S = sh->num_seqs;
   p->H = sh->num_heads;
+  p->Hkv = hkv;
+  p->G = sh->num_heads / hkv;
   p->D = sh->head_dim;
   p->dtype = sh->dtype;
   p->elem_bytes = sh->dtype == KVSEL_BF16 ? 2 : 4;
@@ -267,6 +271,7 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
   a.k = k;
   a.layers = p.layers;
   a.H = p.H;
+  a.kv_group = p.G;
   a.D = p.D;
   a.dtype = p.dtype;
   a.W = W;
@@ -571,6 +576,9 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   sa.status = d->status;
   sa.sm_count = d->sm_count;
   sa.max_prefix = max_prefix(p, W, C);
+  sa.vote_group = 1;
+  sa.kv_H = p.H;
+  sa.kv_div = 1;
   sa.stream = s;
   return cuda_fail(launch_select(sa), "selection launch");
 }
@@ -615,14 +623,24 @@ kvsel_status kvsel_compact(const kvsel_shape* shape, const void* K, const void* 
   if ((double)mr * (double)(ca.row_bytes / 2) > 4.0e9) return KVSEL_ERR_UNSUPPORTED;
   ca.status = d->status;
   ca.sm_count = d->sm_count;
+  ca.kv_H = p.Hkv;
+  ca.kv_div = p.G;
   ca.stream = s;
   return cuda_fail(launch_compact(ca), "gather launch");
 }
 
-kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const void* K,
-                          const void* V, int32_t W, int32_t C, int32_t pool_kind,
-                          int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
-                          void* stream) {
+}  // extern "C"
+
+namespace kvsel {
+namespace {
+
+// The fused path. grouped = 0: one selection per query head (outputs over H
+// heads; query head h gathers K/V head h / G); grouped = 1: one selection per
+// K/V head on the summed votes of its G query heads (outputs over H_kv heads).
+kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void* K,
+                         const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                         int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                         void* stream, bool grouped) {
   Plan p;
   kvsel_status st;
   if (C < 1) return KVSEL_ERR_INVALID_ARG;
@@ -657,7 +675,10 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
   sa.pool_kind = pool_kind;
   sa.pool_k = pool_k;
   sa.layers = p.layers;
-  sa.H = p.H;
+  sa.H = grouped ? p.Hkv : p.H;
+  sa.vote_group = grouped ? p.G : 1;
+  sa.kv_H = p.Hkv;
+  sa.kv_div = grouped ? 1 : p.G;
   sa.W = W;
   sa.C = C;
   sa.T = p.T;
@@ -681,6 +702,27 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
     cudaEventRecord(ev[3], s);
   }
   return KVSEL_OK;
+}
+
+}  // namespace
+}  // namespace kvsel
+
+extern "C" {
+
+kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const void* K,
+                          const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                          int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                          void* stream) {
+  return kvsel::snapkv_impl(shape, q_win, K, V, W, C, pool_kind, pool_k, out_idx, out_K, out_V,
+                            stream, false);
+}
+
+kvsel_status kvsel_snapkv_grouped(const kvsel_shape* shape, const void* q_win, const void* K,
+                                  const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                                  int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                                  void* stream) {
+  return kvsel::snapkv_impl(shape, q_win, K, V, W, C, pool_kind, pool_k, out_idx, out_K, out_V,
+                            stream, true);
 }
 
 kvsel_status kvsel_device_status(void* stream) {

@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(CompactArgs a) {
           const uint32_t s = row / (uint32_t)a.H, h = row - s * (uint32_t)a.H;
           const int32_t j = __ldg(idx + row);
           if (j >= 0 && j < sd.len) {
-            const int64_t src = ((src_tok0 + j) * a.H + h) * a.row_bytes + (int64_t)v * VW;
+            const int64_t src =
+                ((src_tok0 + j) * a.kv_H + h / a.kv_div) * a.row_bytes + (int64_t)v * VW;
             kv[u] = __ldcs(reinterpret_cast<const V*>(kb + src));
             vv[u] = __ldcs(reinterpret_cast<const V*>(vb + src));
             ok[u] = true;

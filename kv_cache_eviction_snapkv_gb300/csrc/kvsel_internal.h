@@ -28,6 +28,7 @@ struct ScoreArgs {
   const void* q;           // q_win
   const void* k;           // K
   int layers, H, D, dtype, W;
+  int kv_group;            // query heads per K head: K head of query head h is h / kv_group
   int64_t T;               // tokens per layer
   int64_t q_rows;          // rows of q_win per layer (num_seqs * W)
   int n_scored;            // number of scored sequences
@@ -77,6 +78,9 @@ struct SelectArgs {
   int slice;               // prefix positions per CTA (set by the launcher)
   int stage_bytes;         // shared bytes before the sort buffer (set by the launcher)
   int gather;              // 1: also copy the kept K/V rows (fused path)
+  int vote_group;          // score planes summed per instance: head h takes planes
+                           // h * vote_group .. + vote_group - 1 of H * vote_group
+  int kv_H, kv_div;        // gather: K/V have kv_H heads; instance head h reads h / kv_div
   const void* k;           // gather: K, V and the compacted outputs
   const void* v;
   void* out_k;
@@ -97,6 +101,7 @@ struct CompactArgs {
   int64_t row_bytes;
   const SeqDesc* seqs;     // every sequence
   int64_t max_rows;        // max over sequences of min(L, C) * H
+  int kv_H, kv_div;        // K/V have kv_H heads; output head h reads h / kv_div
   int* status;
   int sm_count;
   cudaStream_t stream;

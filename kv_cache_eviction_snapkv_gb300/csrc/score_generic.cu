@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(kThreads) generic_score_kernel(ScoreArgs a) {
 
   const int tok = ip.c * a.chunk_tokens + tid;         // position within the sequence
   const bool valid = tok < sd.len;
-  const int64_t krow = (((int64_t)ip.layer * a.T + sd.tok_off + tok) * H + ip.h) * (int64_t)D;
+  const int64_t krow =
+      (((int64_t)ip.layer * a.T + sd.tok_off + tok) * (H / a.kv_group) + ip.h / a.kv_group) *
+      (int64_t)D;
   const int64_t head_plane = (int64_t)ip.layer * H + ip.h;
 
   float vote = 0.f;

@@ -604,7 +604,8 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 #pragma unroll
           for (int hf = 0; hf < kHalves; ++hf)
             tma_load_3d(smem_u32(sk + stage * kStageBytes + hf * kTileM * 128), &P.tmk,
-                        smem_u32(&ms->full[stage]), hf * 64, ip.h, krow0 + t * kTileM, pol_k);
+                        smem_u32(&ms->full[stage]), hf * 64, ip.h / a.kv_group,
+                        krow0 + t * kTileM, pol_k);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == stages) {
@@ -1240,7 +1241,7 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   const size_t smem = fixed + (size_t)stages * kStageBytes;
   TcParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!make_kmap(&p.tmk, a.k, a.D, a.H, (int64_t)a.layers * a.T) ||
+  if (!make_kmap(&p.tmk, a.k, a.D, a.H / a.kv_group, (int64_t)a.layers * a.T) ||
       !make_qmap(&p.tmq, a.q, a.D, a.H, a.W, (int64_t)a.layers * (a.q_rows / a.W), NW))
     return cudaErrorInvalidValue;
   p.a = a;

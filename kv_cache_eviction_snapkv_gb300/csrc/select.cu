@@ -321,7 +321,8 @@ __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int
       const int e = e0 + u * kSelThreads;
       if (e < total) {
         const int s = e / vpr, vi = e - s * vpr;
-        const int64_t src = ((src_tok0 + idx_of(s)) * a.H + h) * a.row_bytes + (int64_t)vi * VW;
+        const int64_t src =
+            ((src_tok0 + idx_of(s)) * a.kv_H + h / a.kv_div) * a.row_bytes + (int64_t)vi * VW;
         kv[u] = __ldcs(reinterpret_cast<const V*>(kb + src));
         vv[u] = __ldcs(reinterpret_cast<const V*>(vb + src));
       }
@@ -559,7 +560,9 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const int j0 = (int)rank * a.slice;                  // slice start
   const int j1 = min(P, j0 + a.slice);                 // slice end (may be <= j0)
   const int n = max(0, j1 - j0);
-  const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sd.tok_off;
+  // the instance's score planes (several when the selection is shared by a
+  // group of heads: their scores are summed in head order)
+  const int64_t plane = ((int64_t)layer * a.H + h) * a.vote_group * a.T + sd.tok_off;
   const float* src = a.scores + plane;
   // the cluster's histogram, result and counts live in the leader
   // the leader's cluster histogram lives in its sort buffer, unused until
@@ -573,7 +576,12 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   // ---- stage the scores with the zero halo; clear the first pass's histograms
   for (int c = tid; c < n + 2 * pad; c += kSelThreads) {
     const int j = j0 - pad + c;
-    stage[c] = (j >= 0 && j < P) ? src[j] : 0.f;
+    float v = 0.f;
+    if (j >= 0 && j < P) {
+      v = src[j];
+      for (int g = 1; g < a.vote_group; ++g) v += src[(int64_t)g * a.T + j];
+    }
+    stage[c] = v;
   }
   for (int i = tid; i < kBins; i += kSelThreads) {
     sh.hist[i] = 0;

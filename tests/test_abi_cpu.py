@@ -105,8 +105,16 @@ def test_other_entry_points_reject_on_host(lib):
     assert lib.kvsel_compact(ctypes.byref(sh.c), None, p, p, 64, p, p, None) == 1
     assert lib.kvsel_window_logits(ctypes.byref(sh.c), p, p, 101, p, None) == 1
     bad = api.Shape(1, 2, 64, api.KVSEL_BF16, [0, 100, 300])
-    bad.c.reserved = 1
+    bad.c.num_kv_heads = 3                       # must divide num_heads
     assert lib.kvsel_window_logits(ctypes.byref(bad.c), p, p, 8, p, None) == 1
+    bad.c.num_kv_heads = -1
+    assert lib.kvsel_snapkv(ctypes.byref(bad.c), p, p, p, 8, 16, 0, 3, p, p, p, None) == 1
+    assert lib.kvsel_snapkv_grouped(ctypes.byref(bad.c), p, p, p, 8, 16, 0, 3, p, p, p,
+                                    None) == 1
+    gqa = api.Shape(1, 4, 64, api.KVSEL_BF16, [0, 100, 300], num_kv_heads=2)
+    assert gqa.c.num_kv_heads == 2
+    assert lib.kvsel_snapkv_grouped(ctypes.byref(gqa.c), p, p, p, 8, 8, 0, 3, p, p, p,
+                                    None) == 1      # C must exceed W
     assert lib.kvsel_set_wait_limit_ns(10) == 1
     assert lib.kvsel_debug_inject(5) == 1
 
