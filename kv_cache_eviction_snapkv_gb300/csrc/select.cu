@@ -497,6 +497,95 @@ __device__ void key_pass4(float* stage, int n, int kind, uint32_t* hist, int* st
   }
 }
 
+// Ascending sort of the k kept composite keys buf[0..k) (~key << 32 |
+// position: larger score first, then smaller position) through buckets of the
+// high word: bucket = (hi - lo) >> s, lo and hi its smallest and largest value,
+// s the smallest shift that maps [lo, hi] onto kBins buckets (for the kept
+// scores of one head, a narrow band of key values). Counts per bucket, an
+// exclusive scan, a scatter into tmp by bucket, then every key is placed at
+// its bucket's start plus the number of smaller keys in its bucket. Returns
+// false, with buf unchanged, when a bucket holds more than kRankMax keys (many
+// equal or clustered scores): the caller sorts another way. Every thread of
+// the block calls it; `cnt` has kBins words; tmp holds k keys.
+constexpr uint32_t kRankMax = 256;
+
+__device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, int k,
+                            uint32_t* cnt, SelShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < k; i += kSelThreads) {
+    const uint32_t w = (uint32_t)(buf[i] >> 32);
+    lo = min(lo, w);
+    hi = max(hi, w);
+  }
+  for (int i = tid; i < kBins; i += kSelThreads) cnt[i] = 0u;
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    sh.warp_cnt[warp][0] = lo;
+    sh.warp_cnt[warp][1] = hi;
+  }
+  __syncthreads();
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+  for (int w = 0; w < kSelWarps; ++w) {
+    lo = min(lo, sh.warp_cnt[w][0]);
+    hi = max(hi, sh.warp_cnt[w][1]);
+  }
+  const uint32_t span = hi - lo;
+  const int sh_bits = span < (uint32_t)kBins ? 0 : (32 - __clz((int)span)) - 11;
+  for (int i = tid; i < k; i += kSelThreads)
+    atomicAdd(&cnt[((uint32_t)(buf[i] >> 32) - lo) >> sh_bits], 1u);
+  __syncthreads();
+  // exclusive scan (thread t owns buckets 4t .. 4t+3) and the largest bucket
+  constexpr int kPer = kBins / kSelThreads;
+  uint32_t c[kPer], tot = 0, mx = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    c[q] = cnt[tid * kPer + q];
+    tot += c[q];
+    mx = max(mx, c[q]);
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 31) sh.warp_cnt[warp][0] = incl;
+  if (lane == 0) sh.warp_cnt[warp][1] = mx;
+  __syncthreads();
+  uint32_t run = incl - tot, biggest = 0;
+  for (int w = 0; w < kSelWarps; ++w) {
+    if (w < warp) run += sh.warp_cnt[w][0];
+    biggest = max(biggest, sh.warp_cnt[w][1]);
+  }
+  if (biggest > kRankMax) return false;   // the same on every thread
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    cnt[tid * kPer + q] = run;
+    run += c[q];
+  }
+  __syncthreads();
+  for (int i = tid; i < k; i += kSelThreads) {
+    const unsigned long long v = buf[i];
+    tmp[atomicAdd(&cnt[((uint32_t)(v >> 32) - lo) >> sh_bits], 1u)] = v;
+  }
+  __syncthreads();
+  // cnt[b] is now the end of bucket b (and the start of b + 1)
+  for (int i = tid; i < k; i += kSelThreads) {
+    const unsigned long long v = tmp[i];
+    const uint32_t b = ((uint32_t)(v >> 32) - lo) >> sh_bits;
+    const int b0 = b ? (int)cnt[b - 1] : 0, b1 = (int)cnt[b];
+    int rank = 0;
+    for (int j = b0; j < b1; ++j) rank += tmp[j] < v;
+    buf[b0 + rank] = v;
+  }
+  __syncthreads();
+  return true;
+}
+
 // Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
 // instance's C: reads their positions from the leader's sorted keys (`sort_r`,
 // its shared window) into `idx`, waits at a cluster barrier (after which the
@@ -520,6 +609,58 @@ __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs
   __syncthreads();
   cluster_sync();
   gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, [&](int s) { return (int)idx[s]; });
+}
+
+// stage[c] = score of position jb + c (summed over `groups` planes T floats
+// apart, in plane order) for c < count, 0 where that position is outside
+// [0, P). Reads whole float4s aligned in memory (the planes share that
+// alignment: T is a multiple of 4 when groups > 1), eight per thread in flight.
+__device__ __forceinline__ void stage_scores_vec(const float* src, int64_t T, int groups,
+                                                 int jb, int count, int P, float* stage) {
+  constexpr int kU = 8;
+  const int mis = (int)(((reinterpret_cast<uintptr_t>(src) >> 2) + (uintptr_t)(intptr_t)jb) & 3u);
+  const int ja = jb - mis;                           // aligned group start (position)
+  const int ng = (count + mis + 3) >> 2;
+  for (int g0 = threadIdx.x; g0 < ng; g0 += kSelThreads * kU) {
+    float4 r[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int g = g0 + u * kSelThreads;
+      const int j = ja + 4 * g;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < ng) {
+        if (j >= 0 && j + 3 < P) {
+          f = __ldcs(reinterpret_cast<const float4*>(src + j));
+          for (int p = 1; p < groups; ++p) {
+            const float4 e = __ldcs(reinterpret_cast<const float4*>(src + p * T + j));
+            f.x += e.x;
+            f.y += e.y;
+            f.z += e.z;
+            f.w += e.w;
+          }
+        } else {
+          float t[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            t[e] = 0.f;
+            if (j + e >= 0 && j + e < P)
+              for (int p = 0; p < groups; ++p) t[e] += src[p * T + j + e];
+          }
+          f = make_float4(t[0], t[1], t[2], t[3]);
+        }
+      }
+      r[u] = f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int g = g0 + u * kSelThreads;
+      const int c = ja + 4 * g - jb;
+      const float t[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (g < ng && c + e >= 0 && c + e < count) stage[c + e] = t[e];
+    }
+  }
 }
 
 template <bool CS1>
@@ -574,14 +715,18 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const uint32_t sort_r = CS1 ? 0u : dsmem_addr(sortbuf, 0);
 
   // ---- stage the scores with the zero halo; clear the first pass's histograms
-  for (int c = tid; c < n + 2 * pad; c += kSelThreads) {
-    const int j = j0 - pad + c;
-    float v = 0.f;
-    if (j >= 0 && j < P) {
-      v = src[j];
-      for (int g = 1; g < a.vote_group; ++g) v += src[(int64_t)g * a.T + j];
+  if (a.vote_group == 1 || (a.T & 3) == 0) {
+    stage_scores_vec(src, a.T, a.vote_group, j0 - pad, n + 2 * pad, P, stage);
+  } else {
+    for (int c = tid; c < n + 2 * pad; c += kSelThreads) {
+      const int j = j0 - pad + c;
+      float v = 0.f;
+      if (j >= 0 && j < P) {
+        v = src[j];
+        for (int g = 1; g < a.vote_group; ++g) v += src[(int64_t)g * a.T + j];
+      }
+      stage[c] = v;
     }
-    stage[c] = v;
   }
   for (int i = tid; i < kBins; i += kSelThreads) {
     sh.hist[i] = 0;
@@ -768,14 +913,14 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   // ---- leader: sort (larger score first, then smaller position), write the
   // slots, then (fused path) copy the kept K/V rows
   const int n2 = kSelThreads * R;
-  for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
-  __syncthreads();
-  if constexpr (R <= 16) {
-    // the staged keys are no longer needed: the stage (sized by the launcher)
-    // is the merge buffer
-    sort_runs_merge<R>(sortbuf, reinterpret_cast<unsigned long long*>(smem));
-  } else {
-    bitonic_sort_blocked<R>(sortbuf, kSelThreads);
+  // the staged keys are no longer needed: the stage (sized by the launcher)
+  // is the scratch of the sorts
+  unsigned long long* scratch = reinterpret_cast<unsigned long long*>(smem);
+  if (R > 16 || !bucket_sort(sortbuf, scratch, (int)k, sh.hist, sh)) {
+    for (int i = (int)k + tid; i < n2; i += kSelThreads) sortbuf[i] = ~0ull;
+    __syncthreads();
+    if constexpr (R <= 16) sort_runs_merge<R>(sortbuf, scratch);
+    else bitonic_sort_blocked<R>(sortbuf, kSelThreads);
   }
   for (int s = tid; s < (int)k; s += kSelThreads)
     out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
