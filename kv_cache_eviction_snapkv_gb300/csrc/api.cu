@@ -116,6 +116,16 @@ struct Carve {
   }
 };
 
+// The selection's stagger words, zeroed on the stream before the launch.
+kvsel_status stagger_words(char* ws, Carve& cv, cudaStream_t s, SelectArgs* sa) {
+  int* w = reinterpret_cast<int*>(ws + cv.take(kSchedWords * sizeof(int)));
+  cudaError_t e = cudaMemsetAsync(w, 0, kSchedWords * sizeof(int), s);
+  if (e) return cuda_fail(e, "cudaMemsetAsync(selection stagger words)");
+  sa->sched = w;
+  sa->stagger_limit_ns = 500000ull;
+  return KVSEL_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Argument rules and the per-call plan
 // ---------------------------------------------------------------------------
@@ -657,8 +667,9 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   if ((st = plan_score(p, W, C, q_win, K, d, &sp))) return st;
   const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
   char* ws;
-  if ((st = workspace(d, score_ws_bytes(p, sp) + 2 * plane_bytes + 2 * 256 +
-                             p.all.size() * sizeof(SeqDesc) + 1024, &ws)))
+  if ((st = workspace(d, score_ws_bytes(p, sp) + 2 * plane_bytes + 3 * 256 +
+                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) + 1024,
+                      &ws)))
     return st;
   Carve cv;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -669,6 +680,7 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   cudaEvent_t* ev = profile_slot();
   if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s, ev))) return st;
   SelectArgs sa{};
+  if ((st = stagger_words(ws, cv, s, &sa))) return st;
   sa.scores = votes;
   sa.pooled_ws = pooled;
   sa.pool_inline = 1;

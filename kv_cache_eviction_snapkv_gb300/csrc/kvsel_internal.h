@@ -87,8 +87,16 @@ struct SelectArgs {
   void* out_v;
   int64_t row_bytes;       // gather: D * element bytes
   int vec_bytes;           // gather: copy width (set by the launcher)
+  int* sched;              // one-CTA instances with the gather: kSchedWords ints zeroed
+                           // before the launch (null: no stagger)
+  unsigned long long stagger_limit_ns;  // longest hold-back of an SM's second CTA
   cudaStream_t stream;
 };
+
+// Selection stagger words: a spare word, then per SM (%smid modulo kSchedSms)
+// the number of CTAs that have started there and a "first selection done" flag.
+constexpr int kSchedSms = 1024;
+constexpr int kSchedWords = 1 + 2 * kSchedSms;
 
 struct CompactArgs {
   const void* k;

@@ -669,9 +669,22 @@ __device__ __forceinline__ void sel_sync() {
   else cluster_sync();
 }
 
+__device__ __forceinline__ void flag_release(int* f) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
+}
+
+__device__ __forceinline__ int flag_acquire(const int* f) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+
+// `selected` (may be null): set by thread 0 once the instance's indices are
+// known, before its rows are copied.
 template <int R, bool CS1>
 __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
-                                unsigned char* smem, SelShared& sh, bool gather_here) {
+                                unsigned char* smem, SelShared& sh, bool gather_here,
+                                int* selected) {
   const int pad = a.pool_inline ? (a.pool_k >> 1) : 0;
   float* stage = reinterpret_cast<float*>(smem);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
@@ -690,6 +703,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
 
   const int cs = CS1 ? 1 : a.cluster;
   if (L < a.C) {  // bypass: keep everything in order, each CTA a share of the rows
+    if (selected && tid == 0) flag_release(selected);
     const int per = (L + cs - 1) / cs, s0 = min(L, (int)rank * per), s1 = min(L, s0 + per);
     for (int s = s0 + tid; s < s1; s += kSelThreads) out[(int64_t)s * a.H] = s;
     if (gather_here)
@@ -925,6 +939,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   for (int s = tid; s < (int)k; s += kSelThreads)
     out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
   for (int w = tid; w < a.W; w += kSelThreads) out[(int64_t)(k + w) * a.H] = P + w;
+  if (selected && tid == 0) flag_release(selected);
   if (!gather_here) return;
   if (CS1) {
     const int kk = (int)k;
@@ -939,12 +954,36 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   }
 }
 
+// Stagger (one-CTA instances with the gather): the two CTAs that start
+// together on an SM would select (on-chip work) and then copy rows (HBM work)
+// in step, and so would every SM, leaving HBM idle while all select. The
+// second CTA to start on an SM therefore waits until the first has selected
+// its instance; from then on one CTA of the pair tends to select while the
+// other copies. The wait is on a CTA that is already running and is bounded
+// (running out of time only costs speed).
 template <int R, bool CS1>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ SelShared sh;
+  int* selected = nullptr;
+  if (CS1 && a.sched && a.gather) {
+    __shared__ int s_slot;
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    sm %= kSchedSms;
+    int* flag = a.sched + 1 + kSchedSms + sm;
+    if (threadIdx.x == 0) {
+      s_slot = atomicAdd(a.sched + 1 + sm, 1);
+      if (s_slot == 1) {
+        const unsigned long long t0 = global_ns();
+        while (!flag_acquire(flag) && global_ns() - t0 < a.stagger_limit_ns) __nanosleep(500);
+      }
+    }
+    __syncthreads();
+    if (s_slot == 0) selected = flag;
+  }
   select_instance<R, CS1>(a, blockIdx.x / a.cluster, CS1 ? 0u : cluster_rank(), smem, sh,
-                          a.gather != 0);
+                          a.gather != 0, selected);
 }
 
 }  // namespace
