@@ -572,7 +572,6 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
   SelectArgs sa{};
   sa.scores = pooled;
-  sa.pooled_ws = nullptr;
   sa.pool_inline = 0;
   sa.layers = p.layers;
   sa.H = p.H;
@@ -667,7 +666,7 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   if ((st = plan_score(p, W, C, q_win, K, d, &sp))) return st;
   const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
   char* ws;
-  if ((st = workspace(d, score_ws_bytes(p, sp) + 2 * plane_bytes + 3 * 256 +
+  if ((st = workspace(d, score_ws_bytes(p, sp) + plane_bytes + 2 * 256 +
                              kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) + 1024,
                       &ws)))
     return st;
@@ -676,13 +675,11 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   const SeqDesc* all_dev;
   if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
   float* votes = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
-  float* pooled = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
   cudaEvent_t* ev = profile_slot();
   if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s, ev))) return st;
   SelectArgs sa{};
   if ((st = stagger_words(ws, cv, s, &sa))) return st;
   sa.scores = votes;
-  sa.pooled_ws = pooled;
   sa.pool_inline = 1;
   sa.pool_kind = pool_kind;
   sa.pool_k = pool_k;

@@ -64,7 +64,6 @@ struct PoolArgs {
 
 struct SelectArgs {
   const float* scores;     // pooled, or votes when pool_inline
-  float* pooled_ws;        // pool_inline: pooled scores written here
   int pool_inline, pool_kind, pool_k;
   int layers, H, W, C;
   int64_t T, T_out;

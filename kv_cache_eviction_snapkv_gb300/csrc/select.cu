@@ -453,11 +453,13 @@ __device__ void sort_runs_merge(unsigned long long* buf, unsigned long long* tmp
 // positions per round (2048 per round, one barrier each), reading their
 // windows as aligned float4s from the zero-padded stage (vote of slice
 // position i at stage[i + K/2]; the stage has 16 floats of slack past its end).
-// Sums and maxima run in increasing position order, as in pool_fixed. Keys go
-// to keys[i] = stage[i] after the round's barrier, counted into `hist` by
-// their top 11 bits.
-template <int K>
-__device__ void key_pass4(float* stage, int n, int kind, uint32_t* hist, int* status) {
+// Sums and maxima run in increasing position order, as in pool_fixed. Average
+// pooling is ranked by the window sum itself: the average is the sum divided
+// by the fixed width k > 0, the same order, and skipping the division keeps
+// sums that differ from rounding to equal averages. Keys go to keys[i] =
+// stage[i] after the round's barrier, counted into `hist` by their top 11 bits.
+template <int K, bool kMaxPool>
+__device__ void key_pass4(float* stage, int n, uint32_t* hist, int* status) {
   constexpr int kW = (K + 3 + 3) / 4;  // float4s covering positions i0 .. i0+3's windows
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t* keys = reinterpret_cast<uint32_t*>(stage);
@@ -477,11 +479,10 @@ __device__ void key_pass4(float* stage, int n, int kind, uint32_t* hist, int* st
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float v;
-      if (kind == KVSEL_POOL_AVG) {
-        float acc = 0.f;
+      if constexpr (!kMaxPool) {
+        v = 0.f;
 #pragma unroll
-        for (int d = 0; d < K; ++d) acc += w[u + d];
-        v = acc / (float)K;
+        for (int d = 0; d < K; ++d) v += w[u + d];
       } else {
         v = w[u];
 #pragma unroll
@@ -750,12 +751,25 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   // ---- keys, counted into the first pass's histogram (top 11 bits) and
   // written at stage index j - j0, over votes no later window needs
   if (a.pool_inline && a.pool_k <= 9) {
+    const bool mx = a.pool_kind != KVSEL_POOL_AVG;
     switch (a.pool_k) {
-      case 1: key_pass4<1>(stage, n, a.pool_kind, sh.hist, a.status); break;
-      case 3: key_pass4<3>(stage, n, a.pool_kind, sh.hist, a.status); break;
-      case 5: key_pass4<5>(stage, n, a.pool_kind, sh.hist, a.status); break;
-      case 7: key_pass4<7>(stage, n, a.pool_kind, sh.hist, a.status); break;
-      default: key_pass4<9>(stage, n, a.pool_kind, sh.hist, a.status); break;
+      case 1: key_pass4<1, false>(stage, n, sh.hist, a.status); break;
+      case 3:
+        if (mx) key_pass4<3, true>(stage, n, sh.hist, a.status);
+        else key_pass4<3, false>(stage, n, sh.hist, a.status);
+        break;
+      case 5:
+        if (mx) key_pass4<5, true>(stage, n, sh.hist, a.status);
+        else key_pass4<5, false>(stage, n, sh.hist, a.status);
+        break;
+      case 7:
+        if (mx) key_pass4<7, true>(stage, n, sh.hist, a.status);
+        else key_pass4<7, false>(stage, n, sh.hist, a.status);
+        break;
+      default:
+        if (mx) key_pass4<9, true>(stage, n, sh.hist, a.status);
+        else key_pass4<9, false>(stage, n, sh.hist, a.status);
+        break;
     }
   } else {
     // one position per thread and chunk (any width, or no pooling)
@@ -780,7 +794,6 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
 
   // ---- three radix passes over (11, 11, 10) bits, summed in the leader
   uint32_t krem = k, prefix = 0;
-  const int n_up = (n + kSelThreads - 1) / kSelThreads * kSelThreads;  // warp-uniform trips
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
     const int nb = pass == 2 ? 1024 : kBins;
@@ -788,13 +801,16 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     if (pass > 0) {
       for (int i = tid; i < nb; i += kSelThreads) sh.hist[i] = 0;
       __syncthreads();
-      for (int i = tid; i < n_up; i += kSelThreads) {
-        uint32_t bin = kNoBin;
-        if (i < n) {
-          const uint32_t key = keys[i];
-          if ((key >> hi_shift) == prefix) bin = (key >> shift) & (uint32_t)(nb - 1);
-        }
-        add_bin(sh.hist, bin, lane);
+      // four keys per thread from one 16-byte read (the stage has slack past
+      // n); the keys left after the first pass spread over the bins, so
+      // plain atomics
+      for (int i4 = 4 * tid; i4 < n; i4 += 4 * kSelThreads) {
+        const uint4 q = *reinterpret_cast<const uint4*>(keys + i4);
+        const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i4 + e < n && (kq[e] >> hi_shift) == prefix)
+            atomicAdd(&sh.hist[(kq[e] >> shift) & (uint32_t)(nb - 1)], 1u);
       }
       __syncthreads();
       if constexpr (!CS1) {
@@ -818,28 +834,31 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   const uint32_t need_eq = krem;    // how many keys equal to thr are kept
 
   // ---- counts of this slice, exchanged through the leader
-  uint32_t my_gt = 0, my_eq = 0;
-  for (int i = tid; i < n; i += kSelThreads) {
-    const uint32_t key = keys[i];
-    my_gt += key > thr;
-    my_eq += key == thr;
-  }
-  my_gt = __reduce_add_sync(0xffffffffu, my_gt);
-  my_eq = __reduce_add_sync(0xffffffffu, my_eq);
-  if (lane == 0) {
-    sh.warp_cnt[warp][0] = my_gt;
-    sh.warp_cnt[warp][1] = my_eq;
-  }
-  __syncthreads();
-  uint32_t slice_gt = 0, slice_eq = 0;
-  for (int w = 0; w < kSelWarps; ++w) {
-    slice_gt += sh.warp_cnt[w][0];
-    slice_eq += sh.warp_cnt[w][1];
-  }
-  uint32_t sel_base = 0, take_eq = 0;
+  uint32_t slice_gt = 0, slice_eq = 0, sel_base = 0, take_eq = 0;
   if constexpr (CS1) {
+    // one slice: the keys above thr are the k - need_eq kept ones, and the
+    // last pass counted the keys equal to thr in the bin of its low bits
+    slice_gt = k - need_eq;
+    slice_eq = sh.hist[thr & 1023u];
     take_eq = min(slice_eq, need_eq);
   } else {
+    uint32_t my_gt = 0, my_eq = 0;
+    for (int i = tid; i < n; i += kSelThreads) {
+      const uint32_t key = keys[i];
+      my_gt += key > thr;
+      my_eq += key == thr;
+    }
+    my_gt = __reduce_add_sync(0xffffffffu, my_gt);
+    my_eq = __reduce_add_sync(0xffffffffu, my_eq);
+    if (lane == 0) {
+      sh.warp_cnt[warp][0] = my_gt;
+      sh.warp_cnt[warp][1] = my_eq;
+    }
+    __syncthreads();
+    for (int w = 0; w < kSelWarps; ++w) {
+      slice_gt += sh.warp_cnt[w][0];
+      slice_eq += sh.warp_cnt[w][1];
+    }
     if (tid == 0) {
       dsmem_st_u32(cnt_r + 8u * rank, slice_gt);
       dsmem_st_u32(cnt_r + 8u * rank + 4u, slice_eq);
