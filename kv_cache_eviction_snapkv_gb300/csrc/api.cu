@@ -213,67 +213,131 @@ int64_t max_prefix(const Plan& p, int W, int C) {
 
 bool gen_supported(int W, int D) { return (int64_t)W * D <= kGenericMaxQ; }
 
-// Scoring plan: the scored sequences (all when C == 0, else L >= C) with
-// their work-item and instance numbering for the chosen kernel.
-struct ScorePlan {
-  bool tc = false;
-  int chunk = 0, wpad = 0;
+// One scoring pass: the scored sequences (all when C == 0, else L >= C) with
+// their work-item and instance numbering for the chosen kernel, and which of
+// the window rows it takes.
+struct ScorePass {
   std::vector<SeqDesc> scored;
   int items_per_layer = 0, inst_per_layer = 0, max_chunks = 0;
+  int chunk = 0, wpad = 0;
+  int W = 0;           // window rows of this pass (its causal mask and statistics)
+  int q_row0 = 0;      // the first of them within each sequence's rows of q_win
+  int vote_cut = 0;    // votes kept for tok < L - W - vote_cut of the pass's L
+  int accumulate = 0;  // added to the votes of the previous pass
 };
 
+struct ScorePlan {
+  bool tc = false;
+  std::vector<ScorePass> passes;
+};
+
+// Window-row split (tensor cores, 32 < W <= 64, long prompts). A selection's
+// votes are a sum over window rows, and every row's softmax is its own, so
+// rows 0 .. 31 (queries P .. P+31, which see only the first P + 32 tokens)
+// and rows 32 .. W-1 can be scored as two instances of at most 32 rows, the
+// second adding its votes to the first's. Each pass keeps at most 32 columns
+// of exponentials per token on chip instead of 64, so the instances of a pass
+// take half the tensor memory and the chunks' statistics exchange overlaps the
+// streaming of K as at W <= 32; the price is reading K twice. (The second
+// pass's padded rows, beyond W, read as zeros, as in a single pass.) Used once
+// an instance exceeds kSplitChunks items of the 64-row kernel.
+constexpr int kSplitChunks = 64;
+
 kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* k,
-                        const DevState* d, ScorePlan* sp) {
+                        const DevState* d, ScorePlan* sp, bool allow_split = true) {
   const bool tc_ok = d->cc_major == 10 && tc_eligible(p.dtype, p.D, W, q, k);
-  auto build = [&](int chunk) {
-    sp->scored.clear();
-    sp->items_per_layer = sp->inst_per_layer = sp->max_chunks = 0;
+  // len_cut: tokens dropped from the end of every sequence (the last rows of
+  // the window that this pass leaves out)
+  auto build = [&](ScorePass& ps, int chunk, int wpad, int len_cut) {
+    ps.scored.clear();
+    ps.items_per_layer = ps.inst_per_layer = ps.max_chunks = 0;
+    ps.chunk = chunk;
+    ps.wpad = wpad;
     for (const SeqDesc& s0 : p.all) {
       if (C > 0 && s0.len < C) continue;
       SeqDesc s = s0;
+      s.len -= len_cut;
       s.n_chunks = (s.len + chunk - 1) / chunk;
       if (s.n_chunks == 0) continue;  // empty sequence (W <= 0 already rejected)
-      s.item_base = sp->items_per_layer;
-      s.inst_base = sp->inst_per_layer;
-      sp->items_per_layer += p.H * s.n_chunks;
-      sp->inst_per_layer += p.H;
-      if (s.n_chunks > sp->max_chunks) sp->max_chunks = s.n_chunks;
-      sp->scored.push_back(s);
+      s.item_base = ps.items_per_layer;
+      s.inst_base = ps.inst_per_layer;
+      ps.items_per_layer += p.H * s.n_chunks;
+      ps.inst_per_layer += p.H;
+      if (s.n_chunks > ps.max_chunks) ps.max_chunks = s.n_chunks;
+      ps.scored.push_back(s);
     }
   };
+  sp->passes.clear();
   if (tc_ok) {
-    build(tc_chunk_tokens(W));
+    ScorePass one;
+    one.W = W;
+    build(one, tc_chunk_tokens(W), tc_window_pad(W), 0);
     // the waits between the chunks of one instance end only if its chunks
     // span at most three rounds of items (chunks <= 2 x CTAs)
-    if (sp->max_chunks <= tc_max_chunks(W, d->sm_count)) {
+    if (one.max_chunks <= tc_max_chunks(W, d->sm_count)) {
       sp->tc = true;
-      sp->chunk = tc_chunk_tokens(W);
-      sp->wpad = tc_window_pad(W);
+      if (allow_split && tc_window_pad(W) == 64 && one.max_chunks > kSplitChunks) {
+        ScorePass a0, a1;
+        a0.W = 32;
+        build(a0, tc_chunk_tokens(32), 32, W - 32);
+        a1.W = W - 32;
+        a1.q_row0 = 32;
+        a1.vote_cut = 32;
+        a1.accumulate = 1;
+        build(a1, tc_chunk_tokens(a1.W), tc_window_pad(a1.W), 0);
+        if (a0.max_chunks <= tc_max_chunks(32, d->sm_count) &&
+            a1.max_chunks <= tc_max_chunks(a1.W, d->sm_count)) {
+          sp->passes.push_back(std::move(a0));
+          sp->passes.push_back(std::move(a1));
+          return KVSEL_OK;
+        }
+      }
+      sp->passes.push_back(std::move(one));
       return KVSEL_OK;
     }
   }
   if (!gen_supported(W, p.D)) return KVSEL_ERR_UNSUPPORTED;
   sp->tc = false;
-  sp->chunk = kGenericChunk;
-  sp->wpad = W;
-  build(kGenericChunk);
+  ScorePass g;
+  g.W = W;
+  build(g, kGenericChunk, W, 0);
+  sp->passes.push_back(std::move(g));
   return KVSEL_OK;
 }
 
-// Uploads the sequence tables and runs the scoring kernels (votes or logits).
+// Uploads the sequence tables and runs the scoring kernels (votes or logits)
+// of every pass of the plan, in order.
+// `ev` (may be null): recorded just before the first pass's kernel and after
+// the last one's.
+kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, DevState* d,
+                      const void* q, const void* k, int W, float* votes, float* logits,
+                      char* ws, Carve& cv, cudaStream_t stream, cudaEvent_t ev_before);
+
 kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const void* q,
                        const void* k, int W, float* votes, float* logits, char* ws,
                        Carve& cv, cudaStream_t stream, cudaEvent_t* ev = nullptr) {
-  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
-  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
+  for (size_t i = 0; i < sp.passes.size(); ++i) {
+    const kvsel_status st = run_pass(p, sp, sp.passes[i], d, q, k, W, votes, logits, ws, cv,
+                                     stream, ev && i == 0 ? ev[0] : nullptr);
+    if (st) return st;
+  }
+  if (ev) cudaEventRecord(ev[1], stream);
+  return KVSEL_OK;
+}
+
+kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, DevState* d,
+                      const void* q, const void* k, int W, float* votes, float* logits,
+                      char* ws, Carve& cv, cudaStream_t stream, cudaEvent_t ev_before) {
+  const int64_t items = (int64_t)p.layers * ps.items_per_layer;
+  const int64_t insts = (int64_t)p.layers * ps.inst_per_layer;
   if (items == 0) return KVSEL_OK;
   if (items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
-  const size_t o_seq = cv.take(sp.scored.size() * sizeof(SeqDesc));
-  const size_t o_part = cv.take((size_t)items * sp.wpad * 2 * sizeof(float));
+  const size_t o_seq = cv.take(ps.scored.size() * sizeof(SeqDesc));
+  const size_t o_part = cv.take((size_t)items * ps.wpad * 2 * sizeof(float));
   const size_t o_cnt = cv.take((size_t)insts * 2 * sizeof(int));
-  const size_t o_fin = cv.take((size_t)insts * sp.wpad * 2 * sizeof(float));
-  cudaError_t e = cudaMemcpyAsync(ws + o_seq, sp.scored.data(),
-                                  sp.scored.size() * sizeof(SeqDesc),
+  const size_t o_fin = cv.take((size_t)insts * ps.wpad * 2 * sizeof(float));
+  cudaError_t e = cudaMemcpyAsync(ws + o_seq, ps.scored.data(),
+                                  ps.scored.size() * sizeof(SeqDesc),
                                   cudaMemcpyHostToDevice, stream);
   if (e) return cuda_fail(e, "cudaMemcpyAsync(sequence table)");
   ScoreArgs a{};
@@ -284,15 +348,19 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
   a.kv_group = p.G;
   a.D = p.D;
   a.dtype = p.dtype;
-  a.W = W;
+  a.W = ps.W;
   a.T = p.T;
   a.q_rows = (int64_t)p.S * W;
-  a.n_scored = (int)sp.scored.size();
+  a.q_W = W;
+  a.q_row0 = ps.q_row0;
+  a.vote_cut = ps.vote_cut;
+  a.accumulate = ps.accumulate;
+  a.n_scored = (int)ps.scored.size();
   a.seqs = reinterpret_cast<const SeqDesc*>(ws + o_seq);
-  a.items_per_layer = sp.items_per_layer;
-  a.inst_per_layer = sp.inst_per_layer;
-  a.chunk_tokens = sp.chunk;
-  a.wpad = sp.wpad;
+  a.items_per_layer = ps.items_per_layer;
+  a.inst_per_layer = ps.inst_per_layer;
+  a.chunk_tokens = ps.chunk;
+  a.wpad = ps.wpad;
   a.scale = (float)(1.0 / std::sqrt((double)p.D));
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
   a.part = reinterpret_cast<float*>(ws + o_part);
@@ -312,21 +380,19 @@ kvsel_status run_score(const Plan& p, const ScorePlan& sp, DevState* d, const vo
   }
   if (sp.tc) {
     // the tensor-core kernel's exchange slots start out as all-ones (empty)
-    if ((e = cudaMemsetAsync(a.part, 0xFF, (size_t)items * sp.wpad * 2 * sizeof(float), stream)))
+    if ((e = cudaMemsetAsync(a.part, 0xFF, (size_t)items * ps.wpad * 2 * sizeof(float), stream)))
       return cuda_fail(e, "cudaMemsetAsync(exchange slots)");
-    if ((e = cudaMemsetAsync(a.final_stats, 0xFF, (size_t)insts * sp.wpad * 2 * sizeof(float),
+    if ((e = cudaMemsetAsync(a.final_stats, 0xFF, (size_t)insts * ps.wpad * 2 * sizeof(float),
                              stream)))
       return cuda_fail(e, "cudaMemsetAsync(final slots)");
     int grid = tc_max_grid(d->sm_count);
     if (items < grid) grid = (int)items;
-    if (ev) cudaEventRecord(ev[0], stream);
+    if (ev_before) cudaEventRecord(ev_before, stream);
     e = launch_tc_score(a, logits != nullptr, grid);
-    if (ev) cudaEventRecord(ev[1], stream);
     return cuda_fail(e, "tensor-core scoring launch");
   }
-  if (ev) cudaEventRecord(ev[0], stream);
+  if (ev_before) cudaEventRecord(ev_before, stream);
   e = launch_generic_score(a, logits != nullptr);
-  if (ev) cudaEventRecord(ev[1], stream);
   return cuda_fail(e, "CUDA-core scoring launch");
 }
 
@@ -341,10 +407,14 @@ kvsel_status upload_all(const Plan& p, char* ws, Carve& cv, cudaStream_t stream,
 }
 
 size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
-  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
-  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
-  return 4096 + sp.scored.size() * sizeof(SeqDesc) + (size_t)items * sp.wpad * 8 +
-         (size_t)insts * 8 + (size_t)insts * sp.wpad * 8 + 4 * 256;
+  size_t total = 4096;
+  for (const ScorePass& ps : sp.passes) {
+    const int64_t items = (int64_t)p.layers * ps.items_per_layer;
+    const int64_t insts = (int64_t)p.layers * ps.inst_per_layer;
+    total += ps.scored.size() * sizeof(SeqDesc) + (size_t)items * ps.wpad * 8 +
+             (size_t)insts * 8 + (size_t)insts * ps.wpad * 8 + 4 * 256;
+  }
+  return total;
 }
 
 }  // namespace
@@ -388,14 +458,16 @@ kvsel_status static_scratch(char** out) {
 
 // Scratch bytes kvsel_score_static carves, in the order it carves them.
 size_t static_score_bytes(const Plan& p, const ScorePlan& sp) {
-  const int64_t items = (int64_t)p.layers * sp.items_per_layer;
-  const int64_t insts = (int64_t)p.layers * sp.inst_per_layer;
   Carve c;
   c.take(p.all.size() * sizeof(SeqDesc) + 1);                 // every sequence
-  c.take(sp.scored.size() * sizeof(SeqDesc));                 // scored sequences
-  c.take((size_t)items * sp.wpad * 2 * sizeof(float));        // exchange slots / partials
-  c.take((size_t)insts * 2 * sizeof(int));                    // counters
-  c.take((size_t)insts * sp.wpad * 2 * sizeof(float));        // merged statistics / slots
+  for (const ScorePass& ps : sp.passes) {
+    const int64_t items = (int64_t)p.layers * ps.items_per_layer;
+    const int64_t insts = (int64_t)p.layers * ps.inst_per_layer;
+    c.take(ps.scored.size() * sizeof(SeqDesc));               // scored sequences
+    c.take((size_t)items * ps.wpad * 2 * sizeof(float));      // exchange slots / partials
+    c.take((size_t)insts * 2 * sizeof(int));                  // counters
+    c.take((size_t)insts * ps.wpad * 2 * sizeof(float));      // merged statistics / slots
+  }
   return c.off;
 }
 
@@ -502,7 +574,7 @@ kvsel_status kvsel_window_logits(const kvsel_shape* shape, const void* q_win, co
   DevState* d;
   if ((st = device_state(&d))) return st;
   ScorePlan sp;
-  if ((st = plan_score(p, W, 0, q_win, K, d, &sp))) return st;
+  if ((st = plan_score(p, W, 0, q_win, K, d, &sp, false))) return st;
   char* ws;
   if ((st = workspace(d, score_ws_bytes(p, sp), &ws))) return st;
   Carve cv;

@@ -498,7 +498,9 @@ __device__ __forceinline__ void rescale_row(uint32_t base, int col, int t, float
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int NW, int KD, bool LOGITS>
+// ACC: add the votes to those already in `votes` (the second pass of a
+// window-row split).
+template <int NW, int KD, bool LOGITS, bool ACC>
 __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcParams P) {
   constexpr int kHalves = KD / 64;
   constexpr int kStageBytes = kTileM * KD * 2;
@@ -570,7 +572,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
                    : "memory");
       const uint64_t pol_k = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      const int seqs_per_layer = (int)(a.q_rows / W);
+      const int seqs_per_layer = (int)(a.q_rows / a.q_W);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -590,7 +592,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf)
           tma_load_4d(smem_u32(sq + qb * kQBytes + hf * NW * 128), &P.tmq,
-                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h, 0,
+                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h, a.q_row0,
                       ip.layer * seqs_per_layer + sd.index, pol_q);
         q_armed |= 1u << qb;
         q_par = (q_par & ~(1u << qb)) | (qp << qb);
@@ -1140,8 +1142,14 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
               p[3] = fmaf(ev[i + 3], c4.w, p[3]);
             }
             const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-            if (tok < sd.len)
-              a.votes[plane + tok] = tok < prefix ? (p[0] + p[1]) + (p[2] + p[3]) : 0.f;
+            if (tok < sd.len) {
+              float v = 0.f;
+              if (tok < prefix - a.vote_cut) {
+                v = (p[0] + p[1]) + (p[2] + p[3]);
+                if constexpr (ACC) v += a.votes[plane + tok];
+              }
+              a.votes[plane + tok] = v;
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -1230,7 +1238,7 @@ bool make_qmap(CUtensorMap* m, const void* base, int D, int H, int W, int64_t se
   return r == CUDA_SUCCESS;
 }
 
-template <int NW, int KD, bool LOGITS>
+template <int NW, int KD, bool LOGITS, bool ACC>
 cudaError_t launch_t(const ScoreArgs& a, int grid) {
   constexpr int kStageBytes = kTileM * KD * 2;
   constexpr int kQBytes = NW * KD * 2;
@@ -1242,12 +1250,12 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   if (!make_kmap(&p.tmk, a.k, a.D, a.H / a.kv_group, (int64_t)a.layers * a.T) ||
-      !make_qmap(&p.tmq, a.q, a.D, a.H, a.W, (int64_t)a.layers * (a.q_rows / a.W), NW))
+      !make_qmap(&p.tmq, a.q, a.D, a.H, a.q_W, (int64_t)a.layers * (a.q_rows / a.q_W), NW))
     return cudaErrorInvalidValue;
   p.a = a;
   p.stages = stages;
   p.n_items = a.layers * a.items_per_layer;
-  auto kern = tc_score_kernel<NW, KD, LOGITS>;
+  auto kern = tc_score_kernel<NW, KD, LOGITS, ACC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1266,14 +1274,25 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
 template <bool LOGITS>
 cudaError_t launch_mode(const ScoreArgs& a, int grid) {
   const int nw = tc_window_pad(a.W);
+  if (a.accumulate) {  // second pass of a split: at most 32 rows, never logits
+    if (LOGITS) return cudaErrorInvalidValue;
+    if (a.D == 128) {
+      if (nw == 16) return launch_t<16, 128, false, true>(a, grid);
+      if (nw == 32) return launch_t<32, 128, false, true>(a, grid);
+    } else if (a.D == 64) {
+      if (nw == 16) return launch_t<16, 64, false, true>(a, grid);
+      if (nw == 32) return launch_t<32, 64, false, true>(a, grid);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.D == 128) {
-    if (nw == 16) return launch_t<16, 128, LOGITS>(a, grid);
-    if (nw == 32) return launch_t<32, 128, LOGITS>(a, grid);
-    if (nw == 64) return launch_t<64, 128, LOGITS>(a, grid);
+    if (nw == 16) return launch_t<16, 128, LOGITS, false>(a, grid);
+    if (nw == 32) return launch_t<32, 128, LOGITS, false>(a, grid);
+    if (nw == 64) return launch_t<64, 128, LOGITS, false>(a, grid);
   } else if (a.D == 64) {
-    if (nw == 16) return launch_t<16, 64, LOGITS>(a, grid);
-    if (nw == 32) return launch_t<32, 64, LOGITS>(a, grid);
-    if (nw == 64) return launch_t<64, 64, LOGITS>(a, grid);
+    if (nw == 16) return launch_t<16, 64, LOGITS, false>(a, grid);
+    if (nw == 32) return launch_t<32, 64, LOGITS, false>(a, grid);
+    if (nw == 64) return launch_t<64, 64, LOGITS, false>(a, grid);
   }
   return cudaErrorInvalidValue;
 }

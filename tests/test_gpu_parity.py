@@ -56,6 +56,9 @@ SCORE_CASES = [
     ("gen_f32_d64", 1, 4, 64, 32, "f32", "avg", 7, [1024, 33]),
     ("gen_bf16_d96", 1, 2, 96, 8, "bf16", "avg", 3, [600, 8]),
     ("gen_w80_d128", 1, 2, 128, 80, "bf16", "avg", 5, [900]),
+    # long prompts at 32 < W <= 64: the window rows are scored in two passes
+    ("tc_w64_split", 1, 2, 128, 64, "bf16", "avg", 7, [40000, 64, 1500]),
+    ("tc_w40_split", 1, 2, 64, 40, "bf16", "max", 5, [33500, 40]),
 ]
 
 
@@ -110,6 +113,7 @@ def test_score_path_choice():
     assert a.kvsel_score_path(sh, 32, 0) == 1
     assert a.kvsel_score_path(sh, 64, 1024) == 1
     assert a.kvsel_score_path(sh, 65, 1024) == 0
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 40000]), 64, 1024) == 1
     assert a.kvsel_score_path(a.Shape(1, 4, 64, a.KVSEL_F32, [0, 5000]), 32, 0) == 0
     assert a.kvsel_score_path(a.Shape(1, 4, 96, a.KVSEL_BF16, [0, 5000]), 32, 0) == 0
 
@@ -246,6 +250,7 @@ E2E_CASES = [
     ("bf16_tc_w16_max", 1, 3, 64, 16, 100, "bf16", "max", 5, [2000, 99, 640]),
     ("f32_generic", 1, 4, 64, 32, 256, "f32", "avg", 7, [1024]),
     ("bf16_tc_w64", 1, 2, 128, 64, 300, "bf16", "avg", 3, [5000, 64, 65]),
+    ("bf16_tc_w64_split", 1, 2, 128, 64, 2048, "bf16", "avg", 7, [36000, 3000, 2047]),
 ]
 
 
