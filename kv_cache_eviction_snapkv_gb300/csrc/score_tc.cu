@@ -1119,6 +1119,19 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
           // its stored exponential times cf_r = 2^(reference_r - M_r -
           // log2 Z_r) (the reference of this lane quarter; 0 for padded
           // rows). This warp takes the tiles of parity `sub`, all rows.
+          const int64_t plane = ((int64_t)ip.layer * a.H + ip.h) * a.T + sd.tok_off;
+          // ACC: the earlier pass's votes of this warp's tokens, loaded before
+          // the wait for the statistics so that their latency overlaps it
+          constexpr int kTpw = ACC ? tiles_per_item(NW) / 2 : 1;
+          float prev[kTpw];
+          if constexpr (ACC) {
+#pragma unroll
+            for (int u = 0; u < kTpw; ++u) {
+              const int t = sub + 2 * u;
+              const int tok = tok0 + t * kTileM + 32 * quarter + lane;
+              prev[u] = (t < ntiles && tok < prefix - a.vote_cut) ? a.votes[plane + tok] : 0.f;
+            }
+          }
           if (ok)
             ok = __all_sync(0xffffffffu,
                             mbar_wait(smem_u32(&ms->ffull[b]), use, limit, abort_flag));
@@ -1127,9 +1140,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
             cf[r] = r < W ? ex2(ms->wm[b][quarter][r] - ms->fin[b][r]) : 0.f;
           __syncwarp();
           mbar_arrive(smem_u32(&ms->fempty[b]));
-          const int64_t plane = ((int64_t)ip.layer * a.H + ip.h) * a.T + sd.tok_off;
-          for (int t = sub; t < ntiles; t += 2) {
-            if (!ok) break;
+          auto vote_tile = [&](int t, float add) {
             float ev[NW];
             tmem_load_row<NW>(item_addr + (uint32_t)(t * NW), ev);
             float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1142,13 +1153,34 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
               p[3] = fmaf(ev[i + 3], c4.w, p[3]);
             }
             const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-            if (tok < sd.len) {
-              float v = 0.f;
-              if (tok < prefix - a.vote_cut) {
-                v = (p[0] + p[1]) + (p[2] + p[3]);
-                if constexpr (ACC) v += a.votes[plane + tok];
+            if (tok < sd.len)
+              a.votes[plane + tok] =
+                  tok < prefix - a.vote_cut ? ((p[0] + p[1]) + (p[2] + p[3])) + add : 0.f;
+          };
+          if constexpr (ACC) {
+#pragma unroll
+            for (int u = 0; u < kTpw; ++u) {
+              const int t = sub + 2 * u;
+              if (ok && t < ntiles) vote_tile(t, prev[u]);
+            }
+          } else {
+            for (int t = sub; t < ntiles; t += 2) {
+              if (!ok) break;
+              float ev[NW];
+              tmem_load_row<NW>(item_addr + (uint32_t)(t * NW), ev);
+              float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int i = 0; i < NW; i += 4) {
+                const float4 c4 = *reinterpret_cast<const float4*>(cf + i);
+                p[0] = fmaf(ev[i], c4.x, p[0]);
+                p[1] = fmaf(ev[i + 1], c4.y, p[1]);
+                p[2] = fmaf(ev[i + 2], c4.z, p[2]);
+                p[3] = fmaf(ev[i + 3], c4.w, p[3]);
               }
-              a.votes[plane + tok] = v;
+              const int tok = tok0 + t * kTileM + 32 * quarter + lane;
+              if (tok < sd.len)
+                a.votes[plane + tok] =
+                    tok < prefix - a.vote_cut ? (p[0] + p[1]) + (p[2] + p[3]) : 0.f;
             }
           }
           tc_fence_before();

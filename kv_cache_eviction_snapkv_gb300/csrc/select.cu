@@ -500,15 +500,24 @@ __device__ void key_pass4(float* stage, int n, uint32_t* hist, int* status) {
 
 // Ascending sort of the k kept composite keys buf[0..k) (~key << 32 |
 // position: larger score first, then smaller position) through buckets of the
-// high word: bucket = (hi - lo) >> s, lo and hi its smallest and largest value,
-// s the smallest shift that maps [lo, hi] onto kBins buckets (for the kept
-// scores of one head, a narrow band of key values). Counts per bucket, an
-// exclusive scan, a scatter into tmp by bucket, then every key is placed at
-// its bucket's start plus the number of smaller keys in its bucket. Returns
-// false, with buf unchanged, when a bucket holds more than kRankMax keys (many
-// equal or clustered scores): the caller sorts another way. Every thread of
-// the block calls it; `cnt` has kBins words; tmp holds k keys.
+// high word w. The kept keys of one head sit in a band [lo, hi] of w (hi is
+// the threshold's), denser towards the threshold, so the bucket of w follows
+// the distance d = hi - w in a floating-point-like code: d itself below 2^mb,
+// above that the position of d's leading bit and the mb bits after it, mb the
+// most that keep the codes of [0, hi - lo] within kBins; bucket = kBins - 1 -
+// code, which rises with w. Counts per bucket, an exclusive scan, a scatter
+// into tmp by bucket, then every key is placed at its bucket's start plus the
+// number of smaller keys in its bucket. Returns false, with buf unchanged,
+// when a bucket holds more than kRankMax keys (many equal or clustered
+// scores): the caller sorts another way. Every thread of the block calls it;
+// `cnt` has kBins words; tmp holds k keys.
 constexpr uint32_t kRankMax = 256;
+
+__device__ __forceinline__ uint32_t dist_code(uint32_t d, int mb) {
+  if (d < (1u << mb)) return d;
+  const int e = (32 - __clz((int)d)) - mb;           // >= 1
+  return ((uint32_t)e << mb) + ((d >> (e - 1)) - (1u << mb));
+}
 
 __device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, int k,
                             uint32_t* cnt, SelShared& sh) {
@@ -533,10 +542,16 @@ __device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, in
     lo = min(lo, sh.warp_cnt[w][0]);
     hi = max(hi, sh.warp_cnt[w][1]);
   }
+  // largest mb whose codes of [0, span] stay below kBins: (B - mb + 1) 2^mb
+  // <= kBins for a span of B bits (B <= 11: every distance its own bucket)
   const uint32_t span = hi - lo;
-  const int sh_bits = span < (uint32_t)kBins ? 0 : (32 - __clz((int)span)) - 11;
-  for (int i = tid; i < k; i += kSelThreads)
-    atomicAdd(&cnt[((uint32_t)(buf[i] >> 32) - lo) >> sh_bits], 1u);
+  const int B = 32 - __clz((int)span);
+  int mb = 10;
+  while (mb > 0 && (B - mb + 1) * (1 << mb) > kBins) --mb;
+  auto bucket = [&](unsigned long long v) {
+    return (uint32_t)(kBins - 1) - dist_code(hi - (uint32_t)(v >> 32), mb);
+  };
+  for (int i = tid; i < k; i += kSelThreads) atomicAdd(&cnt[bucket(buf[i])], 1u);
   __syncthreads();
   // exclusive scan (thread t owns buckets 4t .. 4t+3) and the largest bucket
   constexpr int kPer = kBins / kSelThreads;
@@ -571,13 +586,13 @@ __device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, in
   __syncthreads();
   for (int i = tid; i < k; i += kSelThreads) {
     const unsigned long long v = buf[i];
-    tmp[atomicAdd(&cnt[((uint32_t)(v >> 32) - lo) >> sh_bits], 1u)] = v;
+    tmp[atomicAdd(&cnt[bucket(v)], 1u)] = v;
   }
   __syncthreads();
   // cnt[b] is now the end of bucket b (and the start of b + 1)
   for (int i = tid; i < k; i += kSelThreads) {
     const unsigned long long v = tmp[i];
-    const uint32_t b = ((uint32_t)(v >> 32) - lo) >> sh_bits;
+    const uint32_t b = bucket(v);
     const int b0 = b ? (int)cnt[b - 1] : 0, b1 = (int)cnt[b];
     int rank = 0;
     for (int j = b0; j < b1; ++j) rank += tmp[j] < v;
@@ -589,10 +604,11 @@ __device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, in
 
 // Cluster CTA `rank` of `cs` copies output slots [rank * per, ...) of the
 // instance's C: reads their positions from the leader's sorted keys (`sort_r`,
-// its shared window) into `idx`, waits at a cluster barrier (after which the
-// leader's shared memory may go), then copies the rows.
+// its shared window) into `idx` and writes them to out_idx (`out`, stride H),
+// waits at a cluster barrier (after which the leader's shared memory may go),
+// then copies the rows.
 __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs, uint32_t rank,
-                                  uint32_t sort_r, int32_t* idx, int64_t src_tok0,
+                                  uint32_t sort_r, int32_t* idx, int32_t* out, int64_t src_tok0,
                                   int64_t out_row0, int h) {
   const int per = (a.C + cs - 1) / cs;
   const int s0 = min(a.C, (int)rank * per), s1 = min(a.C, s0 + per);
@@ -606,6 +622,7 @@ __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs
       v = P + (s - (int)k);
     }
     idx[s - s0] = v;
+    out[(int64_t)s * a.H] = v;
   }
   __syncthreads();
   cluster_sync();
@@ -937,8 +954,8 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     // the leader sorts; then every CTA copies a share of the kept rows, its
     // positions read from the leader's sorted keys
     cluster_sync();
-    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), src_tok0,
-                      out_row0, h);
+    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
+                      src_tok0, out_row0, h);
     return;
   }
   if (rank != 0) return;
@@ -955,9 +972,12 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     if constexpr (R <= 16) sort_runs_merge<R>(sortbuf, scratch);
     else bitonic_sort_blocked<R>(sortbuf, kSelThreads);
   }
-  for (int s = tid; s < (int)k; s += kSelThreads)
-    out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
-  for (int w = tid; w < a.W; w += kSelThreads) out[(int64_t)(k + w) * a.H] = P + w;
+  // out_idx: here, unless the cluster's CTAs write it with their copy shares
+  if (CS1 || !gather_here) {
+    for (int s = tid; s < (int)k; s += kSelThreads)
+      out[(int64_t)s * a.H] = (int32_t)(sortbuf[s] & 0xFFFFFFFFull);
+    for (int w = tid; w < a.W; w += kSelThreads) out[(int64_t)(k + w) * a.H] = P + w;
+  }
   if (selected && tid == 0) flag_release(selected);
   if (!gather_here) return;
   if (CS1) {
@@ -968,8 +988,8 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   } else {
     __syncthreads();
     cluster_sync();
-    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), src_tok0,
-                      out_row0, h);
+    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
+                      src_tok0, out_row0, h);
   }
 }
 
