@@ -19,3 +19,10 @@ from .snapkv_oracle import (  # noqa: F401
     window_row_exp_sums,
 )
 from .gqa_oracle import snapkv_group, snapkv_packed_gqa  # noqa: F401,E402
+from .decode_oracle import (  # noqa: F401,E402
+    cache_lengths,
+    decode_attention,
+    decode_packed,
+    decompose,
+    full_probabilities,
+)
