@@ -195,6 +195,57 @@ kvsel_status kvsel_snapkv_grouped(const kvsel_shape* shape, const void* q_win, c
                                   int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
                                   void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Decode-side consumer of a cache (page section "Why deleting positions
+ * changes the output" (删除位置为什么会改变输出): one future query, its softmax
+ * over the cache rows, the value sum, and the probability mass the full cache
+ * gives the kept rows; section "The current prefill still reads the full K/V"
+ * (当前 prefill 仍读完整 K/V，压缩缓存服务后续 decode): after g generated
+ * tokens the cache holds min(L, C) + g rows; section "Cache slots cannot
+ * stand in for the original RoPE positions" (缓存槽位不能代替 RoPE 的原始位置):
+ * the next token's logical position is L + g, its physical slot min(L, C) + g).
+ * ------------------------------------------------------------------------- */
+
+/* One query per (layer, sequence, query head) attends, unmasked, to every row
+ * of its sequence's cache followed by its g appended rows, with the scale
+ * 1/sqrt(D). `shape` describes the cache: seq_offsets are cache row offsets
+ * (for a compacted cache from kvsel_snapkv the running sum of min(L_b, C);
+ * for the full cache the prompt offsets), num_heads the query heads H,
+ * num_kv_heads (0 = H) the cache heads; query head h reads cache head
+ * h / (H / H_kv). Layouts (dtype of the shape, rows of D elements, 16-byte
+ * aligned): q [num_layers][num_seqs][H][D]; K, V [num_layers][T][H_kv][D];
+ * K_new, V_new [num_layers][num_seqs * g][H_kv][D] (sequence b's appended rows
+ * at b*g .. b*g + g - 1; may be NULL when g == 0). Outputs (fp32, caller
+ * owned, device memory): out [num_layers][num_seqs][H][D] the attention
+ * output; lse [num_layers][num_seqs][H] the natural log of the sum of
+ * exp(q . k / sqrt(D)) over the attended rows, or NULL. Permuting a
+ * sequence's cache rows (K and V together) does not change the result, so
+ * kvsel_snapkv's score-ordered rows can be read as they are. Rules:
+ * INVALID_ARG for g < 0, a sequence with no rows at all (cache + g == 0),
+ * NULL or misaligned pointers; UNSUPPORTED for D not in {64, 128}. Device
+ * status: NONFINITE if a sum or an output is not finite. Asynchronous. */
+kvsel_status kvsel_decode_attention(const kvsel_shape* shape, const void* q, const void* K,
+                                    const void* V, int32_t g, const void* K_new,
+                                    const void* V_new, float* out, float* lse, void* stream);
+
+/* Per instance (n of them, e.g. layers * seqs * heads): the retained mass
+ * mass[i] = exp(lse_keep[i] - lse_full[i]) (the full-cache probability of the
+ * rows that the compacted cache kept, when lse_keep comes from the compacted
+ * cache and lse_full from the full one, both with the same appended rows) and
+ * err[i] = || out_full[i] - out_keep[i] ||_2 over the D values. All device
+ * pointers, fp32. INVALID_ARG for n < 0, D < 1 or NULL pointers (n > 0). */
+kvsel_status kvsel_decode_quality(int64_t n, int32_t D, const float* lse_keep,
+                                  const float* lse_full, const float* out_keep,
+                                  const float* out_full, float* mass, float* err, void* stream);
+
+/* Host bookkeeping for a prompt shape (seq_offsets = prompt offsets), budget
+ * C and g appended tokens per sequence: physical_length[b] = min(L_b, C) + g
+ * (also the slot the next token is written to) and next_logical[b] = L_b + g
+ * (its position for RoPE). Host arrays of num_seqs entries. INVALID_ARG for
+ * C < 1, g < 0 or NULL arrays (num_seqs > 0). */
+kvsel_status kvsel_cache_lengths(const kvsel_shape* shape, int32_t C, int32_t g,
+                                 int64_t* physical_length, int64_t* next_logical);
+
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: the first device-side error recorded since the last call, or
  * KVSEL_OK. Returns KVSEL_ERR_CUDA if the synchronisation itself failed. */

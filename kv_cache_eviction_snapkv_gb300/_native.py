@@ -36,6 +36,11 @@ SIGNATURES = {
                              c_vp, c_vp]),
     "kvsel_snapkv_grouped": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
                                      c_vp, c_vp, c_vp]),
+    "kvsel_decode_attention": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                       c_vp]),
+    "kvsel_decode_quality": (c_i32, [c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "kvsel_cache_lengths": (c_i32, [_P, c_i32, c_i32, ctypes.POINTER(c_i64),
+                                    ctypes.POINTER(c_i64)]),
     "kvsel_device_status": (c_i32, [c_vp]),
     "kvsel_set_wait_limit_ns": (c_i32, [c_u64]),
     "kvsel_debug_inject": (c_i32, [c_i32]),

@@ -269,6 +269,66 @@ def kvsel_snapkv_grouped(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: in
     return out_idx, out_K, out_V
 
 
+def kvsel_decode_attention(q, K, V, cache_offsets, K_new=None, V_new=None, g: int = 0,
+                           out=None, lse=None, want_lse: bool = True, stream=None):
+    """(out [layers, S, H, D] fp32, lse [layers, S, H] fp32 or None): one query per
+    (layer, sequence, query head) over its cache rows (packed by cache_offsets)
+    and then its g appended rows. q [layers, S, H, D]; K, V [layers, T, H_kv, D];
+    K_new, V_new [layers, S * g, H_kv, D]."""
+    q4, K4, V4 = q if q.dim() == 4 else q.unsqueeze(0), _as4(K), _as4(V)
+    L, S, H, D = q4.shape
+    if len(cache_offsets) != S + 1:
+        raise ValueError("cache_offsets must have num_seqs + 1 entries")
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q", K4.dtype)
+    sh = Shape(L, H, D, _DTYPES[K4.dtype], cache_offsets, num_kv_heads=K4.shape[2])
+    kn = vn = None
+    if g:
+        kn, vn = _as4(K_new), _as4(V_new)
+        _need(kn, "K_new", K4.dtype), _need(vn, "V_new", K4.dtype)
+    if out is None:
+        out = torch.empty((L, S, H, D), dtype=torch.float32, device=K.device)
+    if lse is None and want_lse:
+        lse = torch.empty((L, S, H), dtype=torch.float32, device=K.device)
+    _need(out, "out", torch.float32)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    _check(_native.lib().kvsel_decode_attention(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(g),
+                                                _ptr(kn), _ptr(vn), _ptr(out), _ptr(lse),
+                                                _stream(stream)), "kvsel_decode_attention")
+    return out, lse
+
+
+def kvsel_decode_quality(lse_keep, lse_full, out_keep, out_full, mass=None, err=None,
+                         stream=None):
+    """(mass, err), each shaped like lse: exp(lse_keep - lse_full) and
+    ||out_full - out_keep||_2 over the last dimension of out."""
+    n = lse_keep.numel()
+    D = out_keep.shape[-1]
+    for t, nm in ((lse_keep, "lse_keep"), (lse_full, "lse_full"), (out_keep, "out_keep"),
+                  (out_full, "out_full")):
+        _need(t, nm, torch.float32)
+    if mass is None:
+        mass = torch.empty_like(lse_keep)
+    if err is None:
+        err = torch.empty_like(lse_keep)
+    _check(_native.lib().kvsel_decode_quality(int(n), int(D), _ptr(lse_keep), _ptr(lse_full),
+                                              _ptr(out_keep), _ptr(out_full), _ptr(mass),
+                                              _ptr(err), _stream(stream)),
+           "kvsel_decode_quality")
+    return mass, err
+
+
+def kvsel_cache_lengths(seq_offsets, C: int, g: int):
+    """(physical_length, next_logical): per sequence min(L_b, C) + g and L_b + g."""
+    sh = Shape(1, 1, 1, KVSEL_BF16, seq_offsets)
+    n = max(0, len(seq_offsets) - 1)
+    phys = (ctypes.c_int64 * max(1, n))()
+    logi = (ctypes.c_int64 * max(1, n))()
+    _check(_native.lib().kvsel_cache_lengths(sh.ref, int(C), int(g), phys, logi),
+           "kvsel_cache_lengths")
+    return [phys[i] for i in range(n)], [logi[i] for i in range(n)]
+
+
 def kvsel_device_status(stream=None) -> int:
     return int(_native.lib().kvsel_device_status(_stream(stream)))
 

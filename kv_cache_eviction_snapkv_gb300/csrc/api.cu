@@ -790,6 +790,125 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
 
 extern "C" {
 
+kvsel_status kvsel_decode_attention(const kvsel_shape* shape, const void* q, const void* K,
+                                    const void* V, int32_t g, const void* K_new,
+                                    const void* V_new, float* out, float* lse, void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if (g < 0) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if (!decode_supported(p.dtype, p.D)) return KVSEL_ERR_UNSUPPORTED;
+  if (p.S == 0) return KVSEL_OK;
+  if (!q || !out || (p.T > 0 && (!K || !V)) || (g > 0 && (!K_new || !V_new)))
+    return KVSEL_ERR_INVALID_ARG;
+  for (const void* ptr : {q, K, V, K_new, V_new})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return KVSEL_ERR_INVALID_ARG;
+  const int chunk = decode_chunk_rows();
+  std::vector<DecSeq> seqs(p.S);
+  int64_t items = 0;
+  for (int b = 0; b < p.S; ++b) {
+    const SeqDesc& sd = p.all[b];
+    const int64_t n = (int64_t)sd.len + g;
+    if (n == 0) return KVSEL_ERR_INVALID_ARG;
+    if (n > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+    DecSeq& d = seqs[b];
+    d.row_off = sd.tok_off;
+    d.n_rows = sd.len;
+    d.n_chunks = (int32_t)((n + chunk - 1) / chunk);
+    d.item_base = (int32_t)items;
+    d.index = b;
+    items += (int64_t)p.H * d.n_chunks;
+    if (items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)p.layers * items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  const size_t part_bytes = (size_t)p.layers * items * (2 + p.D) * sizeof(float);
+  char* ws;
+  if ((st = workspace(d, seqs.size() * sizeof(DecSeq) + part_bytes + 2 * 256, &ws))) return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t o_seq = cv.take(seqs.size() * sizeof(DecSeq));
+  const size_t o_part = cv.take(part_bytes);
+  cudaError_t e = cudaMemcpyAsync(ws + o_seq, seqs.data(), seqs.size() * sizeof(DecSeq),
+                                  cudaMemcpyHostToDevice, s);
+  if (e) return cuda_fail(e, "cudaMemcpyAsync(decode sequence table)");
+  DecodeArgs a{};
+  a.q = q;
+  a.k = K;
+  a.v = V;
+  a.k_new = K_new;
+  a.v_new = V_new;
+  a.layers = p.layers;
+  a.S = p.S;
+  a.H = p.H;
+  a.Hkv = p.Hkv;
+  a.D = p.D;
+  a.dtype = p.dtype;
+  a.g = g;
+  a.T = p.T;
+  a.seqs = reinterpret_cast<const DecSeq*>(ws + o_seq);
+  a.items_per_layer = (int)items;
+  a.chunk_rows = chunk;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
+  a.part = reinterpret_cast<float*>(ws + o_part);
+  a.out = out;
+  a.lse = lse;
+  a.status = d->status;
+  a.stream = s;
+  cudaEvent_t* ev = profile_slot();
+  if (ev) cudaEventRecord(ev[0], s);
+  e = launch_decode(a);
+  if (ev) {
+    cudaEventRecord(ev[1], s);
+    cudaEventRecord(ev[2], s);
+    cudaEventRecord(ev[3], s);
+  }
+  return cuda_fail(e, "decode attention launch");
+}
+
+kvsel_status kvsel_decode_quality(int64_t n, int32_t D, const float* lse_keep,
+                                  const float* lse_full, const float* out_keep,
+                                  const float* out_full, float* mass, float* err, void* stream) {
+  using namespace kvsel;
+  if (n < 0 || D < 1) return KVSEL_ERR_INVALID_ARG;
+  if (n == 0) return KVSEL_OK;
+  if (!lse_keep || !lse_full || !out_keep || !out_full || !mass || !err)
+    return KVSEL_ERR_INVALID_ARG;
+  if (n > 0x7fffffffLL * 8) return KVSEL_ERR_UNSUPPORTED;
+  DevState* d;
+  kvsel_status st;
+  if ((st = device_state(&d))) return st;
+  QualityArgs a{};
+  a.n = n;
+  a.D = D;
+  a.lse_keep = lse_keep;
+  a.lse_full = lse_full;
+  a.out_keep = out_keep;
+  a.out_full = out_full;
+  a.mass = mass;
+  a.err = err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return cuda_fail(launch_decode_quality(a), "decode quality launch");
+}
+
+kvsel_status kvsel_cache_lengths(const kvsel_shape* shape, int32_t C, int32_t g,
+                                 int64_t* physical_length, int64_t* next_logical) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if (C < 1 || g < 0) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if (p.S > 0 && (!physical_length || !next_logical)) return KVSEL_ERR_INVALID_ARG;
+  for (int b = 0; b < p.S; ++b) {
+    const int64_t L = p.all[b].len;
+    physical_length[b] = std::min<int64_t>(L, C) + g;
+    next_logical[b] = L + g;
+  }
+  return KVSEL_OK;
+}
+
 kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const void* K,
                           const void* V, int32_t W, int32_t C, int32_t pool_kind,
                           int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,

@@ -118,6 +118,48 @@ struct CompactArgs {
   cudaStream_t stream;
 };
 
+// Decode-side attention: one query per (layer, sequence, query head) over the
+// sequence's cache rows, then its g appended rows. Work item = (layer,
+// sequence, query head, chunk of chunk_rows rows).
+struct DecSeq {
+  int64_t row_off;         // first cache row of the sequence within a layer
+  int32_t n_rows;          // cache rows (the appended ones come after)
+  int32_t n_chunks;        // chunks per query head
+  int32_t item_base;       // first work item of (this sequence, head 0) within a layer
+  int32_t index;           // sequence number (q row block, appended row block)
+};
+
+struct DecodeArgs {
+  const void* q;           // [layers][S][H][D]
+  const void* k;           // cache [layers][T][Hkv][D]
+  const void* v;
+  const void* k_new;       // appended [layers][S * g][Hkv][D] (g > 0)
+  const void* v_new;
+  int layers, S, H, Hkv, D, dtype, g;
+  int64_t T;               // cache rows per layer
+  const DecSeq* seqs;      // device: every sequence, in order
+  int items_per_layer;
+  int chunk_rows;
+  float scale_log2;        // log2(e) / sqrt(D)
+  float* part;             // [items][2 + D]: base-2 max, sum, weighted values
+  float* out;              // [layers][S][H][D]
+  float* lse;              // [layers][S][H] natural log, or null
+  int* status;
+  cudaStream_t stream;
+};
+
+struct QualityArgs {
+  int64_t n;               // instances
+  int D;
+  const float* lse_keep;
+  const float* lse_full;
+  const float* out_keep;
+  const float* out_full;
+  float* mass;             // exp(lse_keep - lse_full)
+  float* err;              // ||out_full - out_keep||_2
+  cudaStream_t stream;
+};
+
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
 constexpr int64_t kMaxPrefix = 262144;  // longest prefix L - W the select kernel takes
 constexpr int kGenericChunk = 256;   // tokens per CUDA-core scoring block
@@ -128,6 +170,10 @@ cudaError_t launch_generic_score(const ScoreArgs& a, bool logits_mode);
 cudaError_t launch_pool(const PoolArgs& a);
 cudaError_t launch_select(const SelectArgs& a);
 cudaError_t launch_compact(const CompactArgs& a);
+cudaError_t launch_decode(const DecodeArgs& a);
+cudaError_t launch_decode_quality(const QualityArgs& a);
+int decode_chunk_rows();
+bool decode_supported(int dtype, int D);
 
 // Tensor-core path.
 int tc_window_pad(int W);                       // padded MMA N for W, 0 if unsupported

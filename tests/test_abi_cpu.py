@@ -123,3 +123,40 @@ def test_empty_batch_is_a_noop(lib):
     from kv_cache_eviction_snapkv_gb300 import api
     sh = api.Shape(3, 4, 128, api.KVSEL_BF16, [0])
     assert _call_snapkv(lib, sh, 8, 16, ptrs=False) == 0
+
+
+def test_decode_entry_points_host_rules(lib):
+    """Argument rules of the decode entry points (checked before any device work)."""
+    from kv_cache_eviction_snapkv_gb300 import api
+    p = ctypes.c_void_p(256)
+    sh = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 100, 130])
+    assert lib.kvsel_decode_attention(ctypes.byref(sh.c), p, p, p, -1, p, p, p, p, None) == 1
+    assert lib.kvsel_decode_attention(ctypes.byref(sh.c), None, p, p, 0, None, None, p, p,
+                                      None) == 1
+    assert lib.kvsel_decode_attention(ctypes.byref(sh.c), p, p, p, 3, None, None, p, p,
+                                      None) == 1            # g > 0 needs K_new, V_new
+    odd = ctypes.c_void_p(258)
+    assert lib.kvsel_decode_attention(ctypes.byref(sh.c), odd, p, p, 0, None, None, p, p,
+                                      None) == 1            # 16-byte alignment
+    d96 = api.Shape(1, 4, 96, api.KVSEL_BF16, [0, 100])
+    assert lib.kvsel_decode_attention(ctypes.byref(d96.c), p, p, p, 0, None, None, p, p,
+                                      None) == 2            # D not in {64, 128}
+    empty_seq = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 100, 100])
+    assert lib.kvsel_decode_attention(ctypes.byref(empty_seq.c), p, p, p, 0, None, None, p, p,
+                                      None) == 1            # a sequence with no rows at all
+    assert lib.kvsel_decode_quality(-1, 128, p, p, p, p, p, p, None) == 1
+    assert lib.kvsel_decode_quality(5, 0, p, p, p, p, p, p, None) == 1
+    assert lib.kvsel_decode_quality(5, 128, None, p, p, p, p, p, None) == 1
+    assert lib.kvsel_decode_quality(0, 128, None, None, None, None, None, None, None) == 0
+
+
+def test_cache_lengths_follow_the_page(lib):
+    """min(L, C) + g physical rows and L + g logical positions (host only)."""
+    from kv_cache_eviction_snapkv_gb300 import api
+    phys, logi = api.kvsel_cache_lengths([0, 8, 11, 5011], 5, 0)
+    assert phys == [5, 3, 5] and logi == [8, 3, 5000]
+    phys, logi = api.kvsel_cache_lengths([0, 8, 11, 5011], 5, 7)
+    assert phys == [12, 10, 12] and logi == [15, 10, 5007]
+    sh = api.Shape(1, 1, 1, api.KVSEL_BF16, [0, 8])
+    assert lib.kvsel_cache_lengths(ctypes.byref(sh.c), 0, 0, None, None) == 1
+    assert lib.kvsel_cache_lengths(ctypes.byref(sh.c), 5, -1, None, None) == 1
