@@ -28,6 +28,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -45,6 +47,8 @@ def parse_args():
     p.add_argument("--config", default="cfg2")
     p.add_argument("--e2e-steps", type=int, default=4)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-decode", action="store_true",
+                   help="skip the decode-consumer measurement")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-steps", type=int, default=40)
     p.add_argument("--layers", type=int, default=0,
@@ -231,6 +235,75 @@ def score_traffic(layers_full: int):
     return per_capture * layers_full / float(fields["captured_layers"])
 
 
+def measure_decode(api, wl, q_win, k, v, out_k, out_v, dev, peak, peak_kind, iters=20):
+    """Time kvsel_decode_attention on the compacted and the full cache (CUDA
+    events on the launching stream, inputs larger than L2) and report the
+    retained mass and relative output error of the compacted cache."""
+    import torch
+    gen = torch.Generator().manual_seed(4242)
+    q = torch.randn((wl.layers, wl.num_seqs, wl.heads, wl.dim), generator=gen).to(k.dtype).to(dev)
+    kept = [min(l, wl.capacity) for l in wl.seq_lens]
+    kept_offs = [0] + [int(x) for x in np.cumsum(kept)]
+    eb = k.element_size()
+    n = wl.layers * wl.num_seqs * wl.heads
+    o_keep = torch.empty((wl.layers, wl.num_seqs, wl.heads, wl.dim), dtype=torch.float32,
+                         device=dev)
+    o_full = torch.empty_like(o_keep)
+    l_keep = torch.empty((wl.layers, wl.num_seqs, wl.heads), dtype=torch.float32, device=dev)
+    l_full = torch.empty_like(l_keep)
+    io = n * wl.dim * (eb + 4)          # the query in, the output out
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    ms_keep = timed(lambda: api.kvsel_decode_attention(q, out_k, out_v, kept_offs, out=o_keep,
+                                                       lse=l_keep))
+    ms_full = timed(lambda: api.kvsel_decode_attention(q, k, v, wl.offsets, out=o_full,
+                                                       lse=l_full))
+
+    def quality(qq):
+        api.kvsel_decode_attention(qq, out_k, out_v, kept_offs, out=o_keep, lse=l_keep)
+        api.kvsel_decode_attention(qq, k, v, wl.offsets, out=o_full, lse=l_full)
+        mass, err = api.kvsel_decode_quality(l_keep, l_full, o_keep, o_full)
+        m = mass.flatten().double().cpu().numpy()
+        return {"retained_mass": {"mean": float(m.mean()), "min": float(m.min()),
+                                  "p10": float(np.percentile(m, 10))},
+                "output_error": {"mean": float(err.mean()),
+                                 "full_output_norm_mean": float(o_full.norm(dim=-1).mean())}}
+
+    # a query like the window's: the last window query of each (layer, sequence, head)
+    last = torch.arange(wl.num_seqs, device=dev) * wl.window + wl.window - 1
+    q_last = q_win[:, last].contiguous()
+    q_random = quality(q)
+    q_window = quality(q_last)
+    st = api.kvsel_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after decode: {api.kvsel_status_string(st)}")
+
+    def line(ms, rows):
+        b = wl.layers * wl.heads * rows * wl.dim * eb * 2 + io
+        gbs = b / (ms * 1e-3) / 1e9
+        return {"ms": ms, "bytes": b, "achieved_gbs": gbs, "frac": gbs / peak}
+
+    return {"kernels": "decode_partial_kernel + decode_combine_kernel (2 launches per call)",
+            "timed_query": "one N(0,1) query per (layer, sequence, head), g = 0",
+            "compacted": line(ms_keep, sum(kept)), "full": line(ms_full, wl.total),
+            "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+            "quality_random_query": q_random,
+            "quality_last_window_query": q_window,
+            "kept_fraction": sum(kept) / wl.total}
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -328,6 +401,12 @@ def main():
     units = wl.head_tokens()
     value = world * units / (ms * 1e-3)
 
+    # Decode-side consumer: one N(0,1) query per (layer, sequence, head) over the
+    # compacted cache this step produced and over the full prompt cache.
+    decode = None
+    if not args.no_decode:
+        decode = measure_decode(api, wl, q, k, v, out_k, out_v, dev, peak, peak_kind)
+
     # End to end through the public API with host buffers.
     e2e = None
     if not args.no_e2e:
@@ -375,7 +454,9 @@ def main():
                "sample": cpu_pool.sample_text()}
 
     if rank == 0:
-        launches_per_step = 2 if path == 1 else 4   # score kernel(s) + select/gather
+        # score kernel(s) + select/gather: one tensor-core pass, two (row split),
+        # or the CUDA-core statistics, merge and votes kernels
+        launches_per_step = {1: 2, 2: 3}.get(path, 4)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -384,17 +465,22 @@ def main():
             "config": describe(wl),
             "gbs": step_bytes / (ms * 1e-3) / 1e9 * world,
             "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / peak,
-            "roofline": {"bound": "hbm", "kernel": "tc_score_kernel (window logits, softmax "
-                         "statistics, votes)" if path == 1 else "generic scoring kernels",
+            "roofline": {"bound": "hbm", "kernel": {1: "tc_score_kernel (window logits, softmax "
+                                                    "statistics, votes)",
+                                                 2: "tc_score_kernel, two 32-row passes "
+                                                    "(algorithmic bytes count K once)"}.get(
+                                                        path, "generic scoring kernels"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": score_traffic(wl.layers) if path == 1 else None,
+                         "traffic": score_traffic(wl.layers) if path == 1 and
+                         args.config == "cfg2" else None,
                          "bytes_per_launch": score_bytes,
                          "avg_launch_ms": score_ms},
             "stages_ms": {"score": stage_ms[0] / calls, "select_gather": stage_ms[1] / calls,
                           "calls": calls},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "decode": decode,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

@@ -560,7 +560,7 @@ int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C) {
   const void* aligned = reinterpret_cast<const void*>(
       (reinterpret_cast<uintptr_t>(probe) + 255) & ~uintptr_t(255));
   if (plan_score(p, W, C, aligned, aligned, d, &sp) != KVSEL_OK) return -1;
-  return sp.tc ? 1 : 0;
+  return sp.tc ? (sp.passes.size() > 1 ? 2 : 1) : 0;
 }
 
 kvsel_status kvsel_window_logits(const kvsel_shape* shape, const void* q_win, const void* K,

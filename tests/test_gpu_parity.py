@@ -113,7 +113,8 @@ def test_score_path_choice():
     assert a.kvsel_score_path(sh, 32, 0) == 1
     assert a.kvsel_score_path(sh, 64, 1024) == 1
     assert a.kvsel_score_path(sh, 65, 1024) == 0
-    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 40000]), 64, 1024) == 1
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 40000]), 64, 1024) == 2
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 32768]), 64, 1024) == 1
     assert a.kvsel_score_path(a.Shape(1, 4, 64, a.KVSEL_F32, [0, 5000]), 32, 0) == 0
     assert a.kvsel_score_path(a.Shape(1, 4, 96, a.KVSEL_BF16, [0, 5000]), 32, 0) == 0
 
