@@ -197,6 +197,23 @@ kvsel_status kvsel_snapkv_grouped(const kvsel_shape* shape, const void* q_win, c
                                   int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
                                   void* stream);
 
+/* kvsel_snapkv with the cache in host memory: q_win, K, V, out_idx, out_K and
+ * out_V are HOST pointers with kvsel_snapkv's layouts. q_win and K are copied
+ * to the device one layer at a time on an internal copy stream (two device
+ * slots held by the library, so a layer's copy overlaps the previous layer's
+ * kernels); V and the three outputs must be page-locked host memory
+ * (cudaHostAlloc or cudaHostRegister): the gather reads the kept V rows and
+ * writes the outputs in place, so of V only the kept rows cross the link.
+ * Pinned q_win and K copy fastest. Asynchronous and ordered on `stream`: it
+ * starts after the work already queued there, and the outputs are complete
+ * when `stream` reaches the point after the call; the host buffers must stay
+ * valid until then. Rules and limits those of kvsel_snapkv; INVALID_ARG also
+ * when V or an output is not page-locked host memory. */
+kvsel_status kvsel_snapkv_host(const kvsel_shape* shape, const void* q_win, const void* K,
+                               const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                               int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                               void* stream);
+
 /* ---------------------------------------------------------------------------
  * Decode-side consumer of a cache (page section "Why deleting positions
  * changes the output" (删除位置为什么会改变输出): one future query, its softmax

@@ -36,6 +36,8 @@ SIGNATURES = {
                              c_vp, c_vp]),
     "kvsel_snapkv_grouped": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp,
                                      c_vp, c_vp, c_vp]),
+    "kvsel_snapkv_host": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
+                                  c_vp, c_vp]),
     "kvsel_decode_attention": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                        c_vp]),
     "kvsel_decode_quality": (c_i32, [c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),

@@ -269,6 +269,39 @@ def kvsel_snapkv_grouped(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: in
     return out_idx, out_K, out_V
 
 
+def kvsel_snapkv_host(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int, pool_k: int,
+                      out_idx=None, out_K=None, out_V=None, stream=None):
+    """kvsel_snapkv on CPU tensors (V and the outputs pinned): (out_idx, out_K, out_V)
+    pinned CPU tensors, complete once `stream` reaches the point after the call."""
+    K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    for t, n in ((K4, "K"), (V4, "V"), (q4, "q_win")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    if not V4.is_pinned():
+        raise ValueError("V must be pinned (page-locked) host memory")
+    if K4.dtype not in _DTYPES or V4.dtype != K4.dtype or q4.dtype != K4.dtype:
+        raise ValueError("q_win, K and V must share a dtype, bf16 or fp32")
+    sh = shape_of(K, seq_offsets, q4.shape[2])
+    L, H, D = K4.shape[0], q4.shape[2], K4.shape[3]
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_snapkv_host")
+    if out_idx is None:
+        out_idx = torch.empty((L, t_out, H), dtype=torch.int32, pin_memory=True)
+    if out_K is None:
+        out_K = torch.empty((L, t_out, H, D), dtype=K.dtype, pin_memory=True)
+    if out_V is None:
+        out_V = torch.empty((L, t_out, H, D), dtype=K.dtype, pin_memory=True)
+    for t, n in ((out_idx, "out_idx"), (out_K, "out_K"), (out_V, "out_V")):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous pinned CPU tensor")
+    _check(_native.lib().kvsel_snapkv_host(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W), int(C),
+                                           int(pool_kind), int(pool_k), _ptr(out_idx),
+                                           _ptr(out_K), _ptr(out_V), _stream(stream)),
+           "kvsel_snapkv_host")
+    return out_idx, out_K, out_V
+
+
 def kvsel_decode_attention(q, K, V, cache_offsets, K_new=None, V_new=None, g: int = 0,
                            out=None, lse=None, want_lse: bool = True, stream=None):
     """(out [layers, S, H, D] fp32, lse [layers, S, H] fp32 or None): one query per

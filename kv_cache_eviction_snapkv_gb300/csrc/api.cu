@@ -30,6 +30,12 @@ struct DevState {
   int* status = nullptr;        // device address of g_status_word
   char* ws = nullptr;           // workspace
   size_t ws_bytes = 0;
+  // host-buffer path (kvsel_snapkv_host): two device slots for one layer's
+  // q_win and K each, a copy stream and its events
+  char* stage = nullptr;
+  size_t stage_bytes = 0;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t ev_entry = nullptr, ev_loaded[2] = {nullptr, nullptr}, ev_freed[2] = {nullptr, nullptr};
 };
 
 std::mutex g_mu;
@@ -925,6 +931,100 @@ kvsel_status kvsel_snapkv_grouped(const kvsel_shape* shape, const void* q_win, c
                             stream, true);
 }
 
+// Host-buffer path: q_win and K are copied to the device one layer at a time
+// on a copy stream (two slots, so the next layer's copy overlaps this layer's
+// kernels); V and the outputs stay in pinned host memory, read and written in
+// place by the gather (only the kept V rows cross the link).
+kvsel_status kvsel_snapkv_host(const kvsel_shape* shape, const void* q_win, const void* K,
+                               const void* V, int32_t W, int32_t C, int32_t pool_kind,
+                               int32_t pool_k, int32_t* out_idx, void* out_K, void* out_V,
+                               void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if (C < 1) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_budget(W, C))) return st;
+  if ((st = check_pool(pool_kind, pool_k))) return st;
+  if (max_prefix(p, W, C) > kMaxPrefix) return KVSEL_ERR_UNSUPPORTED;
+  if (p.T_out == 0) return KVSEL_OK;
+  if (!q_win || !K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
+  // V and the outputs are read and written by the kernels in place: they
+  // must be page-locked host memory (cudaHostAlloc / cudaHostRegister)
+  void* dev_ptr[4];
+  const void* host_ptr[4] = {V, out_idx, out_K, out_V};
+  for (int i = 0; i < 4; ++i) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, host_ptr[i]) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+        cudaHostGetDevicePointer(&dev_ptr[i], const_cast<void*>(host_ptr[i]), 0) != cudaSuccess) {
+      cudaGetLastError();
+      return KVSEL_ERR_INVALID_ARG;
+    }
+  }
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  const size_t eb = (size_t)p.elem_bytes;
+  const size_t q_layer = (size_t)p.S * W * p.H * p.D * eb;
+  const size_t k_layer = (size_t)p.T * p.Hkv * p.D * eb;
+  const size_t slot = ((q_layer + 255) & ~size_t(255)) + ((k_layer + 255) & ~size_t(255));
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaError_t e;
+    if (d->stage_bytes < 2 * slot) {
+      if (d->stage) {
+        cudaDeviceSynchronize();
+        cudaFree(d->stage);
+        d->stage = nullptr;
+        d->stage_bytes = 0;
+      }
+      if ((e = cudaMalloc(reinterpret_cast<void**>(&d->stage), 2 * slot)))
+        return cuda_fail(e, "cudaMalloc(host-path staging)");
+      d->stage_bytes = 2 * slot;
+    }
+    if (!d->copy) {
+      if ((e = cudaStreamCreateWithFlags(&d->copy, cudaStreamNonBlocking)))
+        return cuda_fail(e, "cudaStreamCreate(copy)");
+      for (cudaEvent_t* ev : {&d->ev_entry, &d->ev_loaded[0], &d->ev_loaded[1], &d->ev_freed[0],
+                              &d->ev_freed[1]})
+        if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)))
+          return cuda_fail(e, "cudaEventCreate");
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // the copies start after the work already queued on the caller's stream
+  if ((e = cudaEventRecord(d->ev_entry, s)) || (e = cudaStreamWaitEvent(d->copy, d->ev_entry, 0)))
+    return cuda_fail(e, "stream ordering");
+  kvsel_shape one = *shape;
+  one.num_layers = 1;
+  const int Hout = p.H;
+  const size_t oi_layer = (size_t)p.T_out * Hout * sizeof(int32_t);
+  const size_t o_layer = (size_t)p.T_out * Hout * p.D * eb;
+  for (int l = 0; l < p.layers; ++l) {
+    const int b = l & 1;
+    char* qd = d->stage + b * slot;
+    char* kd = qd + ((q_layer + 255) & ~size_t(255));
+    if (l >= 2 && (e = cudaStreamWaitEvent(d->copy, d->ev_freed[b], 0)))
+      return cuda_fail(e, "stream ordering");
+    if ((e = cudaMemcpyAsync(qd, static_cast<const char*>(q_win) + l * q_layer, q_layer,
+                             cudaMemcpyHostToDevice, d->copy)) ||
+        (e = cudaMemcpyAsync(kd, static_cast<const char*>(K) + l * k_layer, k_layer,
+                             cudaMemcpyHostToDevice, d->copy)) ||
+        (e = cudaEventRecord(d->ev_loaded[b], d->copy)) ||
+        (e = cudaStreamWaitEvent(s, d->ev_loaded[b], 0)))
+      return cuda_fail(e, "host-path copy");
+    st = snapkv_impl(&one, qd, kd, static_cast<const char*>(dev_ptr[0]) + l * k_layer, W, C,
+                     pool_kind, pool_k,
+                     reinterpret_cast<int32_t*>(static_cast<char*>(dev_ptr[1]) + l * oi_layer),
+                     static_cast<char*>(dev_ptr[2]) + l * o_layer,
+                     static_cast<char*>(dev_ptr[3]) + l * o_layer, stream, false);
+    if (st) return st;
+    if ((e = cudaEventRecord(d->ev_freed[b], s))) return cuda_fail(e, "stream ordering");
+  }
+  return KVSEL_OK;
+}
+
 kvsel_status kvsel_device_status(void* stream) {
   DevState* d;
   kvsel_status st;
@@ -993,12 +1093,13 @@ void kvsel_release(void) {
   int cur = 0;
   cudaGetDevice(&cur);
   for (int i = 0; i < kMaxDevices; ++i) {
-    if (g_dev[i].ws) {
+    if (g_dev[i].ws || g_dev[i].stage) {
       cudaSetDevice(i);
       cudaDeviceSynchronize();
       cudaFree(g_dev[i].ws);
-      g_dev[i].ws = nullptr;
-      g_dev[i].ws_bytes = 0;
+      cudaFree(g_dev[i].stage);
+      g_dev[i].ws = g_dev[i].stage = nullptr;
+      g_dev[i].ws_bytes = g_dev[i].stage_bytes = 0;
     }
   }
   cudaSetDevice(cur);
