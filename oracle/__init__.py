@@ -26,3 +26,10 @@ from .decode_oracle import (  # noqa: F401,E402
     decompose,
     full_probabilities,
 )
+from .jacap_oracle import (  # noqa: F401,E402
+    capacity_matrix,
+    jacap_head,
+    leverage,
+    weights,
+    window_statistics,
+)
