@@ -215,6 +215,37 @@ kvsel_status kvsel_snapkv_host(const kvsel_shape* shape, const void* q_win, cons
                                void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Jacap scorer (pages "Jacap reading notes" / "Jacap technical review",
+ * section 6 (practical approximation) and section 7 (Algorithm 1): per (layer,
+ * sequence, head), over the prefix pool 0 .. P-1 with P = L - W:
+ * z_i = k_i . mu_Q / (tau sqrt(D)), alpha = softmax(z) over the pool,
+ * kappa_i = k_i^T Lambda_Q k_i, w_i = [alpha_i (1 - alpha_i)]^2 kappa_i / D,
+ * A = I + sum_i w_i v_i v_i^T, r_i = w_i v_i^T A^{-1} v_i (the value as the
+ * output proxy); mu_Q and the diagonal Lambda_Q from the W window queries by
+ * the running mean and second moment of section 11 (Algorithm 2) with rate
+ * beta and floor eps, started from the first window query (our reading for a
+ * prompt-time selection). Tensor-core path only: bf16, D = 128, num_kv_heads
+ * equal to num_heads (UNSUPPORTED otherwise). Argument rules of kvsel_score /
+ * kvsel_snapkv plus tau > 0 finite, 0 <= beta < 1, eps >= 0 finite
+ * (INVALID_ARG). Device status: NONFINITE if a statistic or the capacity
+ * matrix is not finite or not positive definite.
+ * ------------------------------------------------------------------------- */
+
+/* Scores r [num_layers][H][T] fp32 (caller owned): r at the prefix positions
+ * of every sequence with L > W, 0 elsewhere. Layouts as kvsel_score. */
+kvsel_status kvsel_jacap_score(const kvsel_shape* shape, const void* q_win, const void* K,
+                               const void* V, int32_t W, float tau, float beta, float eps,
+                               float* scores, void* stream);
+
+/* The whole Jacap path: scores, the top C - W prefix positions by (-r, j) (the
+ * selection of kvsel_select, no pooling), then the window, and the gather of
+ * the kept K and V rows; sequences with L < C are copied unscored. Outputs as
+ * kvsel_snapkv. */
+kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void* K,
+                         const void* V, int32_t W, int32_t C, float tau, float beta, float eps,
+                         int32_t* out_idx, void* out_K, void* out_V, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Decode-side consumer of a cache (page section "Why deleting positions
  * changes the output" (删除位置为什么会改变输出): one future query, its softmax
  * over the cache rows, the value sum, and the probability mass the full cache

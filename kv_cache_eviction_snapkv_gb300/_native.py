@@ -38,6 +38,10 @@ SIGNATURES = {
                                      c_vp, c_vp, c_vp]),
     "kvsel_snapkv_host": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
                                   c_vp, c_vp]),
+    "kvsel_jacap_score": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, ctypes.c_float, ctypes.c_float,
+                                  ctypes.c_float, c_vp, c_vp]),
+    "kvsel_jacap": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, ctypes.c_float, ctypes.c_float,
+                            ctypes.c_float, c_vp, c_vp, c_vp, c_vp]),
     "kvsel_decode_attention": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                        c_vp]),
     "kvsel_decode_quality": (c_i32, [c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),

@@ -269,6 +269,45 @@ def kvsel_snapkv_grouped(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: in
     return out_idx, out_K, out_V
 
 
+def kvsel_jacap_score(q_win, K, V, seq_offsets, W: int, tau: float = 10.0, beta: float = 0.9,
+                      eps: float = 1e-6, scores=None, stream=None):
+    """Jacap leverage scores [layers, H, T] fp32 (prefix positions; 0 elsewhere)."""
+    K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q_win", K4.dtype)
+    L, H = K4.shape[0], q4.shape[2]
+    if scores is None:
+        scores = torch.empty((L, H, sh.T), dtype=torch.float32, device=K.device)
+    _need(scores, "scores", torch.float32)
+    _check(_native.lib().kvsel_jacap_score(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W),
+                                           float(tau), float(beta), float(eps), _ptr(scores),
+                                           _stream(stream)), "kvsel_jacap_score")
+    return scores
+
+
+def kvsel_jacap(q_win, K, V, seq_offsets, W: int, C: int, tau: float = 10.0, beta: float = 0.9,
+                eps: float = 1e-6, out_idx=None, out_K=None, out_V=None, stream=None):
+    """Jacap selection: (out_idx, out_K, out_V) with kvsel_snapkv's layouts."""
+    K4, V4, q4 = _as4(K), _as4(V), _as4(q_win)
+    sh = shape_of(K, seq_offsets, q4.shape[2])
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(q4, "q_win", K4.dtype)
+    L, H, D = K4.shape[0], q4.shape[2], K4.shape[3]
+    t_out = kvsel_out_tokens(sh, C)
+    if t_out < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_jacap")
+    dev = K.device
+    if out_idx is None:
+        out_idx = torch.empty((L, t_out, H), dtype=torch.int32, device=dev)
+    if out_K is None:
+        out_K = torch.empty((L, t_out, H, D), dtype=K.dtype, device=dev)
+    if out_V is None:
+        out_V = torch.empty((L, t_out, H, D), dtype=K.dtype, device=dev)
+    _check(_native.lib().kvsel_jacap(sh.ref, _ptr(q4), _ptr(K4), _ptr(V4), int(W), int(C),
+                                     float(tau), float(beta), float(eps), _ptr(out_idx),
+                                     _ptr(out_K), _ptr(out_V), _stream(stream)), "kvsel_jacap")
+    return out_idx, out_K, out_V
+
+
 def kvsel_snapkv_host(q_win, K, V, seq_offsets, W: int, C: int, pool_kind: int, pool_k: int,
                       out_idx=None, out_K=None, out_V=None, stream=None):
     """kvsel_snapkv on CPU tensors (V and the outputs pinned): (out_idx, out_K, out_V)

@@ -7,6 +7,7 @@
 // capacity and kernel, W <= L, C > W, odd kernel, avg or max pooling; a
 // prompt shorter than the budget bypasses selection (L == C runs the normal
 // path).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -721,6 +722,123 @@ kvsel_status kvsel_compact(const kvsel_shape* shape, const void* K, const void* 
 namespace kvsel {
 namespace {
 
+// Jacap work plan: the scored sequences (L >= max(C, W + 1)) with their
+// statistics, Gram and leverage item numbering (per layer).
+struct JacapPlan {
+  std::vector<JSeq> seqs;
+  int chunks = 0, splits = 0, levs = 0, insts = 0;
+};
+
+JacapPlan plan_jacap(const Plan& p, int W, int C, int sm_count) {
+  JacapPlan jp;
+  int64_t scored_inst = 0;
+  for (const SeqDesc& sd : p.all)
+    if (sd.len >= C && sd.len > W) scored_inst += (int64_t)p.layers * p.H;
+  for (const SeqDesc& sd : p.all) {
+    if (sd.len < C || sd.len <= W) continue;
+    JSeq j{};
+    const int P = sd.len - W;
+    const int n_tiles = (P + 127) / 128;
+    j.tok_off = sd.tok_off;
+    j.len = sd.len;
+    j.index = sd.index;
+    j.n_chunks = (P + kJChunk - 1) / kJChunk;
+    j.chunk_base = jp.chunks;
+    // enough Gram CTAs to fill the GPU, at least one tile each
+    const int64_t want = (sm_count + scored_inst - 1) / std::max<int64_t>(scored_inst, 1);
+    const int split = (int)std::max<int64_t>(1, std::min<int64_t>({want, (int64_t)n_tiles, 64}));
+    const int per = (n_tiles + split - 1) / split;
+    j.n_split = (n_tiles + per - 1) / per;    // every split gets at least one tile
+    j.split_base = jp.splits;
+    j.n_lev = (n_tiles + kJLevTiles - 1) / kJLevTiles;
+    j.lev_base = jp.levs;
+    j.inst_base = jp.insts;
+    jp.chunks += p.H * j.n_chunks;
+    jp.splits += p.H * j.n_split;
+    jp.levs += p.H * j.n_lev;
+    jp.insts += p.H;
+    jp.seqs.push_back(j);
+  }
+  return jp;
+}
+
+size_t jacap_ws_bytes(const Plan& p, const JacapPlan& jp) {
+  const size_t plane = (size_t)p.layers * p.H * p.T;
+  return 8 * 256 + jp.seqs.size() * sizeof(JSeq) + plane * (sizeof(float2) + sizeof(float)) +
+         (size_t)p.layers * jp.chunks * 2 * sizeof(float) +
+         (size_t)p.layers * jp.splits * 128 * 128 * sizeof(float) +
+         (size_t)p.layers * jp.insts * 2 * 128 * 128 * 2;
+}
+
+// Jacap scores into `scores` ([layers][H][T], zeroed first; prefix positions
+// of the planned sequences get r, the rest 0).
+kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const void* q_win,
+                       const void* K, const void* V, int W, float tau, float beta, float eps,
+                       float* scores, char* ws, Carve& cv, cudaStream_t s,
+                       cudaEvent_t* ev = nullptr) {
+  const std::vector<JSeq>& seqs = jp.seqs;
+  const int chunks = jp.chunks, splits = jp.splits, levs = jp.levs, insts = jp.insts;
+  const size_t plane = (size_t)p.layers * p.H * p.T;
+  cudaError_t e = cudaMemsetAsync(scores, 0, plane * sizeof(float), s);
+  if (e) return cuda_fail(e, "cudaMemsetAsync(scores)");
+  if (seqs.empty()) return KVSEL_OK;
+  if ((int64_t)p.layers * std::max({chunks, splits, levs, insts}) > 0x7fffffffLL)
+    return KVSEL_ERR_UNSUPPORTED;
+  const size_t o_seq = cv.take(seqs.size() * sizeof(JSeq));
+  const size_t o_zk = cv.take(plane * sizeof(float2));
+  const size_t o_w = cv.take(plane * sizeof(float));
+  const size_t o_part = cv.take((size_t)p.layers * chunks * 2 * sizeof(float));
+  const size_t o_gram = cv.take((size_t)p.layers * splits * 128 * 128 * sizeof(float));
+  const size_t o_linv = cv.take((size_t)p.layers * insts * 2 * 128 * 128 * 2);
+  if ((e = cudaMemcpyAsync(ws + o_seq, seqs.data(), seqs.size() * sizeof(JSeq),
+                           cudaMemcpyHostToDevice, s)))
+    return cuda_fail(e, "cudaMemcpyAsync(jacap sequence table)");
+  JacapArgs a{};
+  a.q = q_win;
+  a.k = K;
+  a.v = V;
+  a.layers = p.layers;
+  a.H = p.H;
+  a.D = p.D;
+  a.W = W;
+  a.S = p.S;
+  a.T = p.T;
+  a.n_scored = (int)seqs.size();
+  a.seqs = reinterpret_cast<const JSeq*>(ws + o_seq);
+  a.chunks_per_layer = chunks;
+  a.splits_per_layer = splits;
+  a.lev_per_layer = levs;
+  a.inst_per_layer = insts;
+  a.tau = tau;
+  a.beta = beta;
+  a.eps = eps;
+  a.zk = reinterpret_cast<float2*>(ws + o_zk);
+  a.part = reinterpret_cast<float*>(ws + o_part);
+  a.gram = reinterpret_cast<float*>(ws + o_gram);
+  a.wts = reinterpret_cast<float*>(ws + o_w);
+  a.linv = ws + o_linv;
+  a.scores = scores;
+  a.status = d->status;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_limit_ns = g_wait_limit_ns;
+  }
+  a.stream = s;
+  if (ev) cudaEventRecord(ev[0], s);
+  e = launch_jacap(a);
+  if (ev) cudaEventRecord(ev[1], s);
+  return cuda_fail(e, "jacap launch");
+}
+
+kvsel_status check_jacap(const Plan& p, const void* K, const void* V, float tau, float beta,
+                         float eps) {
+  if (!(tau > 0.f) || !(beta >= 0.f && beta < 1.f) || !(eps >= 0.f) || !std::isfinite(tau) ||
+      !std::isfinite(eps))
+    return KVSEL_ERR_INVALID_ARG;
+  if (p.Hkv != p.H || !jacap_eligible(p.dtype, p.D, K, V)) return KVSEL_ERR_UNSUPPORTED;
+  return KVSEL_OK;
+}
+
 // The fused path. grouped = 0: one selection per query head (outputs over H
 // heads; query head h gathers K/V head h / G); grouped = 1: one selection per
 // K/V head on the summed votes of its G query heads (outputs over H_kv heads).
@@ -795,6 +913,92 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
 }  // namespace kvsel
 
 extern "C" {
+
+kvsel_status kvsel_jacap_score(const kvsel_shape* shape, const void* q_win, const void* K,
+                               const void* V, int32_t W, float tau, float beta, float eps,
+                               float* scores, void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if (p.T == 0) return KVSEL_OK;
+  if (!q_win || !K || !V || !scores) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_jacap(p, K, V, tau, beta, eps))) return st;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  const JacapPlan jp = plan_jacap(p, W, 0, d->sm_count);
+  char* ws;
+  if ((st = workspace(d, jacap_ws_bytes(p, jp), &ws))) return st;
+  Carve cv;
+  return run_jacap(p, jp, d, q_win, K, V, W, tau, beta, eps, scores, ws, cv,
+                   static_cast<cudaStream_t>(stream));
+}
+
+kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void* K,
+                         const void* V, int32_t W, int32_t C, float tau, float beta, float eps,
+                         int32_t* out_idx, void* out_K, void* out_V, void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if (C < 1) return KVSEL_ERR_INVALID_ARG;
+  if ((st = plan_shape(shape, C, &p))) return st;
+  if ((st = check_window(p, W))) return st;
+  if ((st = check_budget(W, C))) return st;
+  if (max_prefix(p, W, C) > kMaxPrefix) return KVSEL_ERR_UNSUPPORTED;
+  if (p.T_out == 0) return KVSEL_OK;
+  if (!q_win || !K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_jacap(p, K, V, tau, beta, eps))) return st;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
+  const JacapPlan jp = plan_jacap(p, W, C, d->sm_count);
+  char* ws;
+  if ((st = workspace(d, jacap_ws_bytes(p, jp) + plane_bytes + 2 * 256 +
+                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) + 1024,
+                      &ws)))
+    return st;
+  Carve cv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqDesc* all_dev;
+  if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
+  float* scores = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
+  cudaEvent_t* ev = profile_slot();
+  if ((st = run_jacap(p, jp, d, q_win, K, V, W, tau, beta, eps, scores, ws, cv, s, ev)))
+    return st;
+  SelectArgs sa{};
+  if ((st = stagger_words(ws, cv, s, &sa))) return st;
+  sa.scores = scores;
+  sa.pool_inline = 0;
+  sa.layers = p.layers;
+  sa.H = p.H;
+  sa.vote_group = 1;
+  sa.kv_H = p.H;
+  sa.kv_div = 1;
+  sa.W = W;
+  sa.C = C;
+  sa.T = p.T;
+  sa.T_out = p.T_out;
+  sa.n_seqs = p.S;
+  sa.seqs = all_dev;
+  sa.out_idx = out_idx;
+  sa.status = d->status;
+  sa.sm_count = d->sm_count;
+  sa.max_prefix = max_prefix(p, W, C);
+  sa.gather = 1;
+  sa.k = K;
+  sa.v = V;
+  sa.out_k = out_K;
+  sa.out_v = out_V;
+  sa.row_bytes = (int64_t)p.D * p.elem_bytes;
+  sa.stream = s;
+  if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
+  if (ev) {
+    cudaEventRecord(ev[2], s);
+    cudaEventRecord(ev[3], s);
+  }
+  return KVSEL_OK;
+}
 
 kvsel_status kvsel_decode_attention(const kvsel_shape* shape, const void* q, const void* K,
                                     const void* V, int32_t g, const void* K_new,

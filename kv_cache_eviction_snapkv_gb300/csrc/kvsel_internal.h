@@ -160,6 +160,46 @@ struct QualityArgs {
   cudaStream_t stream;
 };
 
+// Jacap scoring (leverage of the value directions under the capacity matrix).
+// Instance = (layer, scored sequence, head); its pool is the prefix 0 .. P-1.
+struct JSeq {
+  int64_t tok_off;         // first token of the sequence within a layer
+  int32_t len;             // L
+  int32_t index;           // sequence number in the call (q_win row block)
+  int32_t n_chunks;        // statistics chunks (kJChunk prefix rows each)
+  int32_t chunk_base;      // first statistics item of (sequence, head 0) within a layer
+  int32_t n_split;         // Gram splits per head
+  int32_t split_base;      // first Gram item of (sequence, head 0) within a layer
+  int32_t n_lev;           // leverage items per head (kJLevTiles tiles each)
+  int32_t lev_base;        // first leverage item of (sequence, head 0) within a layer
+  int32_t inst_base;       // instance id of (sequence, head 0) within a layer
+  int32_t pad;
+};
+
+struct JacapArgs {
+  const void* q;           // q_win [layers][S * W][H][D] bf16
+  const void* k;           // [layers][T][H][D] bf16
+  const void* v;
+  int layers, H, D, W, S;  // S: sequences in the call (q_win blocks)
+  int64_t T;
+  int n_scored;
+  const JSeq* seqs;        // device: the scored sequences
+  int chunks_per_layer, splits_per_layer, lev_per_layer, inst_per_layer;
+  float tau, beta, eps;
+  float2* zk;              // [layers][H][T]: (z in base-2 units, kappa) per prefix token
+  float* part;             // [statistics items][2]: base-2 max and sum of 2^z
+  float* gram;             // [Gram items][D][D] partial sums of w v v^T
+  float* wts;              // [layers][H][T]: w per prefix token
+  void* linv;              // [instances][2][D][D] bf16: L^{-1} split into hi + lo
+  float* scores;           // [layers][H][T]: r per prefix token
+  int* status;
+  unsigned long long wait_limit_ns;
+  cudaStream_t stream;
+};
+
+constexpr int kJChunk = 512;         // prefix rows per statistics item
+constexpr int kJLevTiles = 8;        // 128-token tiles per leverage item
+
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
 constexpr int64_t kMaxPrefix = 262144;  // longest prefix L - W the select kernel takes
 constexpr int kGenericChunk = 256;   // tokens per CUDA-core scoring block
@@ -171,6 +211,8 @@ cudaError_t launch_pool(const PoolArgs& a);
 cudaError_t launch_select(const SelectArgs& a);
 cudaError_t launch_compact(const CompactArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a);
+cudaError_t launch_jacap(const JacapArgs& a);
+bool jacap_eligible(int dtype, int D, const void* k, const void* v);
 cudaError_t launch_decode_quality(const QualityArgs& a);
 int decode_chunk_rows();
 bool decode_supported(int dtype, int D);

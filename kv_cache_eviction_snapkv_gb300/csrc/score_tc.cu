@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "kvsel_device.cuh"
+#include "tc_common.cuh"
 
 namespace kvsel {
 namespace {
@@ -97,60 +98,6 @@ struct Misc {
   alignas(16) float cf[kEpiWarps][64];   // pass C factors of each epilogue warp
 };
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase with `parity`; gives up when the limit passes or
-// (if `abort_flag` is non-null) when another role has given up.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            unsigned long long limit_ns,
-                                            const volatile int* abort_flag) {
-  const unsigned long long t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 31) == 0) {
-      if (abort_flag && *abort_flag) return false;
-      if (global_ns() - t0 > limit_ns) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          unsigned long long limit_ns,
-                                          const volatile int* abort_flag) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, limit_ns, abort_flag);
-}
-
 // Row statistics slots of the cross-chunk exchange: one 8-byte (reference,
 // sum) pair per (work item, row), pre-filled with an all-ones pattern (a NaN
 // reference, which a published pair never has). A relaxed 8-byte store is
@@ -191,213 +138,6 @@ __device__ __forceinline__ void slot_read2(const unsigned long long* p0,
       "ld.relaxed.gpu.global.b64 %1, [%3];"
       : "=l"(v[0]), "=l"(v[1])
       : "l"(p0), "l"(p1));
-}
-
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from global to shared memory, completing on mbarrier `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart (SBO); version field 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;             // LBO (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;   // SBO
-  d |= (uint64_t)1 << 46;             // descriptor version
-  d |= (uint64_t)2 << 61;             // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: D fp32, A and B bf16, both K-major, N and M.
-__host__ __device__ constexpr uint32_t instr_desc(int n, int m) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
-
-#define KVSEL_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
-                    "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : KVSEL_R8(0), KVSEL_R8(8)
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : KVSEL_R8(0), KVSEL_R8(8), KVSEL_R8(16), KVSEL_R8(24)
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// After tcgen05.wait::ld: ties each loaded value to an empty volatile asm that
-// follows the wait, so no use of the value can be scheduled before the wait.
-template <int N>
-__device__ __forceinline__ void after_wait(float (&v)[N]) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
-}
-
-template <int NW>
-__device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&v)[NW]) {
-  if constexpr (NW == 16) {
-    tmem_ld16(taddr, v);
-  } else {
-#pragma unroll
-    for (int c = 0; c < NW; c += 32) tmem_ld32(taddr + c, v + c);
-  }
-  tmem_wait_ld();
-  after_wait(v);
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : KVSEL_R8(0)
-               : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// One column, no wait (tcgen05.wait::ld and after_wait must follow).
-__device__ __forceinline__ float tmem_ld1_nowait(uint32_t taddr) {
-  uint32_t r;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-  return __uint_as_float(r);
-}
-
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-  float v[1] = {tmem_ld1_nowait(taddr)};
-  tmem_wait_ld();
-  after_wait(v);
-  return v[0];
-}
-
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
-               "r"(__float_as_uint(v))
-               : "memory");
-}
-
-#define KVSEL_W8(i) "r"(__float_as_uint(v[i])), "r"(__float_as_uint(v[i + 1])), \
-                    "r"(__float_as_uint(v[i + 2])), "r"(__float_as_uint(v[i + 3])), \
-                    "r"(__float_as_uint(v[i + 4])), "r"(__float_as_uint(v[i + 5])), \
-                    "r"(__float_as_uint(v[i + 6])), "r"(__float_as_uint(v[i + 7]))
-
-// Stores N consecutive TMEM columns of this thread's lane (N = 8, 16 or 32).
-template <int N>
-__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)[N]) {
-  if constexpr (N == 8) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 ::"r"(taddr), KVSEL_W8(0) : "memory");
-  } else if constexpr (N == 16) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                 ::"r"(taddr), KVSEL_W8(0), KVSEL_W8(8) : "memory");
-  } else {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                 ::"r"(taddr), KVSEL_W8(0), KVSEL_W8(8), KVSEL_W8(16), KVSEL_W8(24)
-                 : "memory");
-  }
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// N consecutive TMEM columns of this thread's lane (N = 8, 16 or 32).
-template <int N>
-__device__ __forceinline__ void tmem_load_cols_nowait(uint32_t taddr, float* v) {
-  if constexpr (N == 8) tmem_ld8(taddr, v);
-  else if constexpr (N == 16) tmem_ld16(taddr, v);
-  else tmem_ld32(taddr, v);
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[N]) {
-  tmem_load_cols_nowait<N>(taddr, v);
-  tmem_wait_ld();
-  after_wait(v);
-}
-
-
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "l"(policy)
-      : "memory");
 }
 
 // (m1, z1) merged with (m2, z2), sums relative to the merged max.
@@ -1225,20 +965,6 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
 
 // K as (D, H, rows): box of 64 elements x 1 head x 128 tokens.
 bool make_kmap(CUtensorMap* m, const void* base, int D, int H, int64_t rows) {

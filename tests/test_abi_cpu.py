@@ -160,3 +160,27 @@ def test_cache_lengths_follow_the_page(lib):
     sh = api.Shape(1, 1, 1, api.KVSEL_BF16, [0, 8])
     assert lib.kvsel_cache_lengths(ctypes.byref(sh.c), 0, 0, None, None) == 1
     assert lib.kvsel_cache_lengths(ctypes.byref(sh.c), 5, -1, None, None) == 1
+
+
+def test_jacap_host_rules(lib):
+    """Jacap argument rules and the tensor-path limits, checked on the host."""
+    from kv_cache_eviction_snapkv_gb300 import api
+    p = ctypes.c_void_p(256)
+    f = ctypes.c_float
+    sh = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 1000, 1500])
+    assert lib.kvsel_jacap_score(ctypes.byref(sh.c), p, p, p, 0, f(10), f(0.9), f(1e-6), p,
+                                 None) == 1                      # W = 0
+    assert lib.kvsel_jacap_score(ctypes.byref(sh.c), p, p, p, 8, f(0), f(0.9), f(1e-6), p,
+                                 None) == 1                      # tau
+    assert lib.kvsel_jacap_score(ctypes.byref(sh.c), p, p, p, 8, f(10), f(1.0), f(1e-6), p,
+                                 None) == 1                      # beta
+    assert lib.kvsel_jacap_score(ctypes.byref(sh.c), p, p, p, 8, f(10), f(0.5), f(-1), p,
+                                 None) == 1                      # eps
+    d64 = api.Shape(1, 4, 64, api.KVSEL_BF16, [0, 1000])
+    assert lib.kvsel_jacap_score(ctypes.byref(d64.c), p, p, p, 8, f(10), f(0.9), f(1e-6), p,
+                                 None) == 2                      # D = 64: no tensor path
+    gqa = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 1000], num_kv_heads=2)
+    assert lib.kvsel_jacap_score(ctypes.byref(gqa.c), p, p, p, 8, f(10), f(0.9), f(1e-6), p,
+                                 None) == 2                      # grouped K/V heads
+    assert lib.kvsel_jacap(ctypes.byref(sh.c), p, p, p, 8, 8, f(10), f(0.9), f(1e-6), p, p, p,
+                           None) == 1                            # C <= W
