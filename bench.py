@@ -49,6 +49,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-decode", action="store_true",
                    help="skip the decode-consumer measurement")
+    p.add_argument("--no-jacap", action="store_true", help="skip the Jacap measurement")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-steps", type=int, default=40)
     p.add_argument("--layers", type=int, default=0,
@@ -304,6 +305,50 @@ def measure_decode(api, wl, q_win, k, v, out_k, out_v, dev, peak, peak_kind, ite
             "kept_fraction": sum(kept) / wl.total}
 
 
+def measure_jacap(api, wl, q_win, k, v, dev, peak, peak_kind, iters=10):
+    """Time kvsel_jacap_score (statistics, Gram, factor and leverage kernels) and
+    the fused kvsel_jacap (plus the selection and gather) with CUDA events."""
+    import torch
+    tau, beta, eps = 10.0, 0.9, 1e-6
+    scores = torch.empty((wl.layers, wl.heads, wl.total), dtype=torch.float32, device=dev)
+    kept = wl.out_tokens
+    oi = torch.empty((wl.layers, kept, wl.heads), dtype=torch.int32, device=dev)
+    ok_ = torch.empty((wl.layers, kept, wl.heads, wl.dim), dtype=k.dtype, device=dev)
+    ov_ = torch.empty_like(ok_)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    ms_score = timed(lambda: api.kvsel_jacap_score(q_win, k, v, wl.offsets, wl.window, tau,
+                                                   beta, eps, scores=scores))
+    ms_full = timed(lambda: api.kvsel_jacap(q_win, k, v, wl.offsets, wl.window, wl.capacity,
+                                            tau, beta, eps, oi, ok_, ov_))
+    st = api.kvsel_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after jacap: {api.kvsel_status_string(st)}")
+    eb = k.element_size()
+    prefix = sum(max(0, l - wl.window) for l in wl.seq_lens)
+    # K read once (statistics), V twice (Gram, leverage), the scores written
+    b = wl.layers * wl.heads * prefix * (3 * wl.dim * eb + 4)
+    flops = wl.layers * wl.heads * prefix * (2 * wl.dim * wl.dim) * 3   # Gram + 2 leverage MMAs
+    gbs = b / (ms_score * 1e-3) / 1e9
+    return {"kernels": "jacap_stats, jacap_gram (tcgen05), jacap_factor, jacap_leverage "
+                       "(tcgen05)", "tau": tau, "beta": beta, "eps": eps,
+            "score_ms": ms_score, "bytes": b, "achieved_gbs": gbs, "frac": gbs / peak,
+            "peak": peak, "peak_source": peak_kind, "tensor_tflops": flops / (ms_score * 1e-3) / 1e12,
+            "fused_ms": ms_full, "fused_head_tokens_per_s": wl.head_tokens() / (ms_full * 1e-3)}
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -407,6 +452,11 @@ def main():
     if not args.no_decode:
         decode = measure_decode(api, wl, q, k, v, out_k, out_v, dev, peak, peak_kind)
 
+    # Jacap scorer on the same inputs (bf16, D = 128 only).
+    jacap = None
+    if not args.no_jacap and wl.dtype == "bf16" and wl.dim == 128:
+        jacap = measure_jacap(api, wl, q, k, v, dev, peak, peak_kind)
+
     # End to end through the C ABI with host buffers: kvsel_snapkv_host copies
     # q_win and K to the device layer by layer and reads the kept V rows and
     # writes the outputs in place in pinned host memory.
@@ -482,6 +532,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "decode": decode,
+            "jacap": jacap,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

@@ -830,12 +830,12 @@ kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const vo
   return cuda_fail(e, "jacap launch");
 }
 
-kvsel_status check_jacap(const Plan& p, const void* K, const void* V, float tau, float beta,
-                         float eps) {
+kvsel_status check_jacap(const Plan& p, const void* q, const void* K, const void* V, float tau,
+                         float beta, float eps) {
   if (!(tau > 0.f) || !(beta >= 0.f && beta < 1.f) || !(eps >= 0.f) || !std::isfinite(tau) ||
       !std::isfinite(eps))
     return KVSEL_ERR_INVALID_ARG;
-  if (p.Hkv != p.H || !jacap_eligible(p.dtype, p.D, K, V)) return KVSEL_ERR_UNSUPPORTED;
+  if (p.Hkv != p.H || !jacap_eligible(p.dtype, p.D, q, K, V)) return KVSEL_ERR_UNSUPPORTED;
   return KVSEL_OK;
 }
 
@@ -924,7 +924,7 @@ kvsel_status kvsel_jacap_score(const kvsel_shape* shape, const void* q_win, cons
   if ((st = check_window(p, W))) return st;
   if (p.T == 0) return KVSEL_OK;
   if (!q_win || !K || !V || !scores) return KVSEL_ERR_INVALID_ARG;
-  if ((st = check_jacap(p, K, V, tau, beta, eps))) return st;
+  if ((st = check_jacap(p, q_win, K, V, tau, beta, eps))) return st;
   DevState* d;
   if ((st = device_state(&d))) return st;
   const JacapPlan jp = plan_jacap(p, W, 0, d->sm_count);
@@ -948,7 +948,7 @@ kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void
   if (max_prefix(p, W, C) > kMaxPrefix) return KVSEL_ERR_UNSUPPORTED;
   if (p.T_out == 0) return KVSEL_OK;
   if (!q_win || !K || !V || !out_idx || !out_K || !out_V) return KVSEL_ERR_INVALID_ARG;
-  if ((st = check_jacap(p, K, V, tau, beta, eps))) return st;
+  if ((st = check_jacap(p, q_win, K, V, tau, beta, eps))) return st;
   DevState* d;
   if ((st = device_state(&d))) return st;
   const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);

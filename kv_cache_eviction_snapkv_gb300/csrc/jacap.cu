@@ -54,6 +54,7 @@ __device__ __forceinline__ int find_jseq(const JacapArgs& a, int rem, F base_of)
 __global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant__ JacapArgs a) {
   __shared__ float mu_s[kJD], lam_s[kJD];
   __shared__ float wm[8], wl[8];
+  __shared__ __align__(16) __nv_bfloat16 qs[32][kJD];   // 32 window queries at a time
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int item = blockIdx.x;
   const int layer = item / a.chunks_per_layer;
@@ -63,17 +64,37 @@ __global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant_
   const int h = local / sq.n_chunks, c = local - h * sq.n_chunks;
   const int P = sq.len - a.W;
   const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  if (tid < kJD) {
+  {
+    // the window statistics: rows staged 32 at a time with every thread
+    // loading (16 bytes each), the recursion run by one thread per dimension
     const int64_t row0 = (int64_t)layer * a.S * a.W + (int64_t)sq.index * a.W;
-    float mu = __bfloat162float(qb[(row0 * a.H + h) * kJD + tid]);
-    float m2 = mu * mu;
-    for (int r = 1; r < a.W; ++r) {
-      const float q = __bfloat162float(qb[((row0 + r) * a.H + h) * kJD + tid]);
-      mu = a.beta * mu + (1.f - a.beta) * q;
-      m2 = a.beta * m2 + (1.f - a.beta) * (q * q);
+    float mu = 0.f, m2 = 0.f;
+    for (int r0 = 0; r0 < a.W; r0 += 32) {
+      const int nr = min(32, a.W - r0);
+      for (int e = tid; e < nr * (kJD / 8); e += blockDim.x) {
+        const int r = e / (kJD / 8), c = e - r * (kJD / 8);
+        *reinterpret_cast<uint4*>(&qs[r][c * 8]) = *reinterpret_cast<const uint4*>(
+            qb + ((row0 + r0 + r) * a.H + h) * kJD + c * 8);
+      }
+      __syncthreads();
+      if (tid < kJD) {
+        for (int r = 0; r < nr; ++r) {
+          const float q = __bfloat162float(qs[r][tid]);
+          if (r0 + r == 0) {
+            mu = q;
+            m2 = q * q;
+          } else {
+            mu = a.beta * mu + (1.f - a.beta) * q;
+            m2 = a.beta * m2 + (1.f - a.beta) * (q * q);
+          }
+        }
+      }
+      __syncthreads();
     }
-    mu_s[tid] = mu * (1.4426950408889634f / (a.tau * sqrtf((float)kJD)));
-    lam_s[tid] = fmaxf(m2 - mu * mu, a.eps);
+    if (tid < kJD) {
+      mu_s[tid] = mu * (1.4426950408889634f / (a.tau * sqrtf((float)kJD)));
+      lam_s[tid] = fmaxf(m2 - mu * mu, a.eps);
+    }
   }
   __syncthreads();
   const int grp = lane >> 3, sub = lane & 7;
@@ -152,9 +173,8 @@ struct GramSmem {
   unsigned long long drain;                    // abort path: the MMA issuer's last commit
   uint32_t tmem_base;
   int abort_flag;
-  int tr_abort;                                // transposers: one of them gave up
   float norm_m, norm_s;                        // the instance's base-2 softmax max and sum
-  float sw[kJTile];                            // sqrt(w) of the current tile's tokens
+  float sw[2][kJTile];                         // sqrt(w) of a tile's tokens (double buffer)
 };
 
 struct GramParams {
@@ -164,6 +184,21 @@ struct GramParams {
 
 __device__ __forceinline__ void work_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGWork) : "memory");
+}
+
+// Barrier of the transposing threads that also returns, in every one of them,
+// whether any passed `v` true.
+__device__ __forceinline__ bool work_bar_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kGWork)
+      : "memory");
+  return r != 0;
 }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 64-column
@@ -209,7 +244,6 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
     mbar_init(smem_u32(&ms->done), 1);
     mbar_init(smem_u32(&ms->drain), 1);
     ms->abort_flag = 0;
-    ms->tr_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -301,66 +335,76 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
     work_bar();
     const float nm = ms->norm_m, inv_s = 1.f / ms->norm_s;
     const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sq.tok_off;
-    const int tb = tid >> 4, db = tid & 15;      // 8 tokens x 8 dimensions per thread
+    // sqrt(w) of a tile's tokens into sw[buf] (threads 0..127, one token each)
+    auto weights_of = [&](int tile, int buf) {
+      if (tid < kJTile) {
+        const int t = tile * kJTile + tid;
+        float w = 0.f;
+        if (t < P) {
+          const float2 zk = a.zk[plane + t];
+          const float al = ex2(zk.x - nm) * inv_s;
+          const float g = al * (1.f - al);
+          w = g * g * zk.y * (1.f / kJD);
+          a.wts[plane + t] = w;
+        }
+        ms->sw[buf][tid] = sqrtf(w);
+      }
+    };
+    if (n_my > 0) weights_of(t_begin, 0);
+    work_bar();
+    // transposition by 8 x 8 blocks: warp wq takes dimension blocks 2wq, 2wq+1
+    // and, per step, token blocks 2p, 2p+1 (four blocks: one ldmatrix.x4.trans
+    // from the V tile, one stmatrix.x4 into the transposed buffer; each 8-row
+    // phase of either touches eight distinct chunks of a swizzle period)
+    const int wq = tid >> 5, lid = tid & 31;
+    const int m_of = lid >> 3, r_of = lid & 7;          // the matrix and row this lane addresses
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0; i < n_my; ++i) {
       const int b = i & 1;
-      const int tok0 = (t_begin + i) * kJTile;
-      if (tid < kJTile) {
-        const int t = tok0 + tid;
-        float sw = 0.f;
-        if (t < P) {
-          const float2 zk = a.zk[plane + t];
-          const float al = ex2(zk.x - nm) * inv_s;
-          const float g = al * (1.f - al);
-          const float w = g * g * zk.y * (1.f / kJD);
-          a.wts[plane + t] = w;
-          sw = sqrtf(w);
-        }
-        ms->sw[tid] = sw;
-      }
+      if (i + 1 < n_my) weights_of(t_begin + i + 1, (i + 1) & 1);
       bool mine = mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag);
       if (mine && i >= 2)
         mine = mbar_wait(smem_u32(&ms->tempty[b]), (uint32_t)((i - 2) >> 1) & 1, limit, abort_flag);
-      if (!mine) ms->tr_abort = 1;
-      work_bar();                              // sw[] written, waits done by everyone
-      if (ms->tr_abort) {                      // the same value in every transposer
+      if (mine) {
+        const uint32_t vt = smem_u32(sv + stage * kJTileBytes);
+        const uint32_t tt = smem_u32(st + b * kJTileBytes);
+        const float* sw = ms->sw[i & 1];
+#pragma unroll 2
+        for (int pstep = 0; pstep < 8; ++pstep) {
+          // this lane's address: matrix m_of = (token block 2p + m/2, dimension block 2wq + m%2)
+          const int tbl = 2 * pstep + (m_of >> 1), dbl = 2 * wq + (m_of & 1);
+          const uint32_t src = vt + (dbl >> 3) * kAtom + swz(tbl * 8 + r_of, dbl & 7);
+          uint32_t rg[4];
+          asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(rg[0]), "=r"(rg[1]), "=r"(rg[2]), "=r"(rg[3])
+                       : "r"(src)
+                       : "memory");
+          // register m holds, for dimension dbl*8 + lid/4, tokens (lid%4)*2 and +1 of
+          // token block 2p + m/2: scale each by its sqrt(w)
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int t0 = (2 * pstep + (m >> 1)) * 8 + (lid & 3) * 2;
+            const float f0 = sw[t0], f1 = sw[t0 + 1];
+            const float x0 = __uint_as_float(rg[m] << 16), x1 = __uint_as_float(rg[m] & 0xFFFF0000u);
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(f0 != 0.f ? f0 * x0 : 0.f,
+                                                            f1 != 0.f ? f1 * x1 : 0.f);
+            rg[m] = *reinterpret_cast<const uint32_t*>(&p2);
+          }
+          // stored matrix m_of: rows = dimensions dbl*8 .., 8 tokens of block tbl
+          const uint32_t dst = tt + (tbl >> 3) * kAtom + swz(dbl * 8 + r_of, tbl & 7);
+          asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst),
+                       "r"(rg[0]), "r"(rg[1]), "r"(rg[2]), "r"(rg[3])
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      // the tile written by all, or a wait given up somewhere (same answer everywhere)
+      if (work_bar_any(!mine)) {
         ok = false;
         break;
       }
-      // V tile (token rows, 2 atoms of 64 dimensions) -> sqrt(w) V^T (dimension
-      // rows, 2 atoms of 64 tokens)
-      const unsigned char* vt = sv + stage * kJTileBytes;
-      unsigned char* tt = st + b * kJTileBytes;
-      float x[8][8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int t = tb * 8 + r;
-        const uint4 q = *reinterpret_cast<const uint4*>(vt + (db >> 3) * kAtom + swz(t, db & 7));
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-        const float f = ms->sw[t];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)   // tokens outside the pool (f = 0) give exact zeros
-          x[r][e] = f != 0.f ? f * __uint_as_float((e & 1) ? (u[e >> 1] & 0xFFFF0000u)
-                                                          : (u[e >> 1] << 16))
-                             : 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int d = db * 8 + e;
-        uint32_t pk[4];
-#pragma unroll
-        for (int r = 0; r < 8; r += 2) {
-          const __nv_bfloat162 p2 = __floats2bfloat162_rn(x[r][e], x[r + 1][e]);
-          pk[r >> 1] = *reinterpret_cast<const uint32_t*>(&p2);
-        }
-        *reinterpret_cast<uint4*>(tt + (tb >> 3) * kAtom + swz(d, tb & 7)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      work_bar();
       if (tid == 0) {
         mbar_arrive(smem_u32(&ms->tfull[b]));
         mbar_arrive(smem_u32(&ms->empty[stage]));
@@ -425,8 +469,8 @@ constexpr int kFLd = kJD + 1;                  // padded row of the fp32 matrice
 
 __global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
   extern __shared__ float fs[];
-  float* A = fs;                               // [kJD][kFLd], lower triangle used
-  float* X = fs + kJD * kFLd;                  // L^{-1}
+  float* A = fs;                               // [kJD][kFLd]: A, then L in the lower triangle
+  float* X = fs + kJD * kFLd;                  // L^{-1} (lower triangle)
   __shared__ int bad;
   const int tid = threadIdx.x;
   const int inst = blockIdx.x;
@@ -436,48 +480,81 @@ __global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant
   const int h = rem - sq.inst_base;
   const int64_t g0 = (int64_t)layer * a.splits_per_layer + sq.split_base + (int64_t)h * sq.n_split;
   if (tid == 0) bad = 0;
-  for (int e = tid; e < kJD * kJD; e += blockDim.x) {
-    const int i = e / kJD, j = e - i * kJD;
-    if (j > i) continue;
-    float acc = i == j ? 1.f : 0.f;
-    for (int s = 0; s < sq.n_split; ++s) acc += a.gram[(g0 + s) * kJD * kJD + e];
-    A[i * kFLd + j] = acc;
+  // A = I + the partial Grams (fixed order), lower triangle
+  {
+    const float* __restrict__ gp = a.gram + g0 * kJD * kJD;
+    constexpr int kPer = kJD * kJD / 256;       // elements per thread (every 256th)
+    float acc[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * 256;
+      acc[q] = (e >> 7) == (e & (kJD - 1)) ? 1.f : 0.f;
+    }
+    const int nsp = sq.n_split;
+    for (int sp = 0; sp < nsp; ++sp) {         // every load of a partial in flight at once
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) acc[q] += __ldg(gp + (int64_t)sp * kJD * kJD + tid + q * 256);
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * 256, i = e >> 7, j = e & (kJD - 1);
+      if (j <= i) A[i * kFLd + j] = acc[q];
+    }
   }
   __syncthreads();
-  for (int k = 0; k < kJD; ++k) {
-    if (tid == 0) {
-      const float p = A[k * kFLd + k];
-      if (!(p > 0.f) || !finite_f(p)) bad = 1;
-      A[k * kFLd + k] = sqrtf(fmaxf(p, 1e-30f));
+  // two threads per row (or column) of each step, each taking every other k
+  // of the dot product with four accumulators; the halves are added by a
+  // shuffle
+  const int pair = tid >> 1, half = tid & 1;
+  auto dot = [&](const float* x, int xs, const float* y, int ys, int k0, int k1) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int k = k0 + half;
+    for (; k + 6 < k1; k += 8) {
+      s0 = fmaf(x[k * xs], y[k * ys], s0);
+      s1 = fmaf(x[(k + 2) * xs], y[(k + 2) * ys], s1);
+      s2 = fmaf(x[(k + 4) * xs], y[(k + 4) * ys], s2);
+      s3 = fmaf(x[(k + 6) * xs], y[(k + 6) * ys], s3);
     }
-    __syncthreads();
-    const float piv = A[k * kFLd + k];
-    for (int i = k + 1 + tid; i < kJD; i += blockDim.x) A[i * kFLd + k] /= piv;
-    __syncthreads();
-    // trailing update of the lower triangle: rows i > k, columns k < j <= i
-    const int n = kJD - 1 - k;
-    for (int e = tid; e < n * n; e += blockDim.x) {
-      const int i = k + 1 + e / n, j = k + 1 + e % n;
-      if (j <= i) A[i * kFLd + j] -= A[i * kFLd + k] * A[j * kFLd + k];
-    }
-    __syncthreads();
-  }
-  // X = L^{-1}, column by column (forward substitution)
-  for (int c = tid; c < kJD; c += blockDim.x) {
-    for (int i = 0; i < c; ++i) X[i * kFLd + c] = 0.f;
-    X[c * kFLd + c] = 1.f / A[c * kFLd + c];
-    for (int i = c + 1; i < kJD; ++i) {
+    for (; k < k1; k += 2) s0 = fmaf(x[k * xs], y[k * ys], s0);
+    float acc = (s0 + s1) + (s2 + s3);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    return acc;
+  };
+  // Cholesky, left-looking, one column at a time: L[j][j] = sqrt(A[j][j] -
+  // sum_k L[j][k]^2), then L[i][j] = (A[i][j] - sum_{k<j} L[i][k] L[j][k]) /
+  // L[j][j] for the rows below
+  for (int j = 0; j < kJD; ++j) {
+    if (tid < 32) {                            // the diagonal: one warp, a strided dot product
       float acc = 0.f;
-      for (int k = c; k < i; ++k) acc = fmaf(A[i * kFLd + k], X[k * kFLd + c], acc);
-      X[i * kFLd + c] = -acc / A[i * kFLd + i];
+      for (int k = tid; k < j; k += 32) acc = fmaf(A[j * kFLd + k], A[j * kFLd + k], acc);
+      for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (tid == 0) {
+        const float p = A[j * kFLd + j] - acc;
+        if (!(p > 0.f) || !finite_f(p)) bad = 1;
+        A[j * kFLd + j] = sqrtf(fmaxf(p, 1e-30f));
+      }
     }
+    __syncthreads();
+    const float inv = 1.f / A[j * kFLd + j];
+    const int i = j + 1 + pair;                // rows j+1 .. 127 (pairs of threads)
+    const float acc = dot(A + (i < kJD ? i : j) * kFLd, 1, A + j * kFLd, 1, 0, j);
+    if (i < kJD && half == 0) A[i * kFLd + j] = (A[i * kFLd + j] - acc) * inv;
+    __syncthreads();
   }
-  __syncthreads();
+  // X = L^{-1}, one row at a time: X[i][i] = 1 / L[i][i] and, for c < i,
+  // X[i][c] = -(sum_{k=c}^{i-1} L[i][k] X[k][c]) / L[i][i], a column per pair
+  for (int i = 0; i < kJD; ++i) {
+    const float inv = 1.f / A[i * kFLd + i];
+    const int c = pair;                        // columns 0 .. 127
+    const float acc = dot(A + i * kFLd, 1, X + c, kFLd, c, c <= i ? i : c);
+    if (c <= i && half == 0) X[i * kFLd + c] = c == i ? inv : -acc * inv;
+    __syncthreads();
+  }
   __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(a.linv) + (int64_t)inst * 2 * kJD * kJD;
   __nv_bfloat16* lo = hi + kJD * kJD;
   for (int e = tid; e < kJD * kJD; e += blockDim.x) {
-    const int i = e / kJD, j = e - i * kJD;
-    const float x = X[i * kFLd + j];
+    const int r = e >> 7, c = e & (kJD - 1);
+    const float x = c <= r ? X[r * kFLd + c] : 0.f;
     const __nv_bfloat16 xh = __float2bfloat16_rn(x);
     hi[e] = xh;
     lo[e] = __float2bfloat16_rn(x - __bfloat162float(xh));
@@ -718,9 +795,11 @@ constexpr size_t lev_smem() {
 
 }  // namespace
 
-bool jacap_eligible(int dtype, int D, const void* k, const void* v) {
+bool jacap_eligible(int dtype, int D, const void* q, const void* k, const void* v) {
   if (dtype != KVSEL_BF16 || D != kJD) return false;
-  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return false;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v)) & 15)
+    return false;
   return encode_fn() != nullptr;
 }
 

@@ -212,7 +212,7 @@ cudaError_t launch_select(const SelectArgs& a);
 cudaError_t launch_compact(const CompactArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_jacap(const JacapArgs& a);
-bool jacap_eligible(int dtype, int D, const void* k, const void* v);
+bool jacap_eligible(int dtype, int D, const void* q, const void* k, const void* v);
 cudaError_t launch_decode_quality(const QualityArgs& a);
 int decode_chunk_rows();
 bool decode_supported(int dtype, int D);
