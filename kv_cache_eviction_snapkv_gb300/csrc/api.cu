@@ -726,14 +726,15 @@ namespace {
 // statistics, Gram and leverage item numbering (per layer).
 struct JacapPlan {
   std::vector<JSeq> seqs;
-  int chunks = 0, splits = 0, levs = 0, insts = 0;
+  int chunks = 0, insts = 0;
+  // Gram work: pieces, the pieces of each CTA and of each instance
+  std::vector<JSeg> segs;
+  std::vector<int32_t> cta_seg, inst_seg;
 };
 
 JacapPlan plan_jacap(const Plan& p, int W, int C, int sm_count) {
   JacapPlan jp;
-  int64_t scored_inst = 0;
-  for (const SeqDesc& sd : p.all)
-    if (sd.len >= C && sd.len > W) scored_inst += (int64_t)p.layers * p.H;
+  std::vector<int> tiles_of;                   // per scored sequence
   for (const SeqDesc& sd : p.all) {
     if (sd.len < C || sd.len <= W) continue;
     JSeq j{};
@@ -744,29 +745,60 @@ JacapPlan plan_jacap(const Plan& p, int W, int C, int sm_count) {
     j.index = sd.index;
     j.n_chunks = (P + kJChunk - 1) / kJChunk;
     j.chunk_base = jp.chunks;
-    // enough Gram CTAs to fill the GPU, at least one tile each
-    const int64_t want = (sm_count + scored_inst - 1) / std::max<int64_t>(scored_inst, 1);
-    const int split = (int)std::max<int64_t>(1, std::min<int64_t>({want, (int64_t)n_tiles, 64}));
-    const int per = (n_tiles + split - 1) / split;
-    j.n_split = (n_tiles + per - 1) / per;    // every split gets at least one tile
-    j.split_base = jp.splits;
-    j.n_lev = (n_tiles + kJLevTiles - 1) / kJLevTiles;
-    j.lev_base = jp.levs;
     j.inst_base = jp.insts;
     jp.chunks += p.H * j.n_chunks;
-    jp.splits += p.H * j.n_split;
-    jp.levs += p.H * j.n_lev;
     jp.insts += p.H;
     jp.seqs.push_back(j);
+    tiles_of.push_back(n_tiles);
   }
+  if (jp.seqs.empty()) return jp;
+  // Gram: every instance's tiles in instance order (layer, sequence, head),
+  // cut into n_gram equal contiguous ranges, each range into pieces at the
+  // instance boundaries
+  const int64_t n_inst = (int64_t)p.layers * jp.insts;
+  std::vector<int64_t> start(n_inst + 1, 0);
+  {
+    int64_t i = 0;
+    for (int layer = 0; layer < p.layers; ++layer)
+      for (size_t q = 0; q < jp.seqs.size(); ++q)
+        for (int h = 0; h < p.H; ++h, ++i) start[i + 1] = start[i] + tiles_of[q];
+  }
+  const int64_t total = start[n_inst];
+  const int64_t n_gram = std::max<int64_t>(
+      1, std::min<int64_t>(sm_count, total / kJGramMinTiles));
+  jp.cta_seg.assign(n_gram + 1, 0);
+  jp.inst_seg.assign(n_inst + 1, 0);
+  int64_t inst = 0;
+  for (int64_t c = 0; c < n_gram; ++c) {
+    int64_t lo = c * total / n_gram;
+    const int64_t hi = (c + 1) * total / n_gram;
+    while (lo < hi) {
+      while (start[inst + 1] <= lo) ++inst;
+      const int64_t end = std::min(hi, start[inst + 1]);
+      if (lo == start[inst]) jp.inst_seg[inst] = (int32_t)jp.segs.size();
+      jp.segs.push_back(JSeg{(int32_t)inst, (int32_t)(lo - start[inst]),
+                             (int32_t)(end - start[inst]), 0});
+      lo = end;
+    }
+    jp.cta_seg[c + 1] = (int32_t)jp.segs.size();
+  }
+  jp.inst_seg[n_inst] = (int32_t)jp.segs.size();
   return jp;
+}
+
+// The tables the kernels read, packed for one host-to-device copy: sequences,
+// pieces, the CTAs' and the instances' piece ranges.
+size_t jacap_table_bytes(const JacapPlan& jp) {
+  auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+  return up16(jp.seqs.size() * sizeof(JSeq)) + up16(jp.segs.size() * sizeof(JSeg)) +
+         up16(jp.cta_seg.size() * sizeof(int32_t)) + up16(jp.inst_seg.size() * sizeof(int32_t));
 }
 
 size_t jacap_ws_bytes(const Plan& p, const JacapPlan& jp) {
   const size_t plane = (size_t)p.layers * p.H * p.T;
-  return 8 * 256 + jp.seqs.size() * sizeof(JSeq) + plane * (sizeof(float2) + sizeof(float)) +
-         (size_t)p.layers * jp.chunks * 2 * sizeof(float) +
-         (size_t)p.layers * jp.splits * 128 * 128 * sizeof(float) +
+  return 8 * 256 + plane * (sizeof(float2) + sizeof(float)) +
+         (size_t)p.layers * jp.chunks * 2 * sizeof(float) + jacap_table_bytes(jp) +
+         jp.segs.size() * 128 * 128 * sizeof(float) +
          (size_t)p.layers * jp.insts * 2 * 128 * 128 * 2;
 }
 
@@ -777,22 +809,37 @@ kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const vo
                        float* scores, char* ws, Carve& cv, cudaStream_t s,
                        cudaEvent_t* ev = nullptr) {
   const std::vector<JSeq>& seqs = jp.seqs;
-  const int chunks = jp.chunks, splits = jp.splits, levs = jp.levs, insts = jp.insts;
+  const int chunks = jp.chunks, insts = jp.insts;
   const size_t plane = (size_t)p.layers * p.H * p.T;
   cudaError_t e = cudaMemsetAsync(scores, 0, plane * sizeof(float), s);
   if (e) return cuda_fail(e, "cudaMemsetAsync(scores)");
   if (seqs.empty()) return KVSEL_OK;
-  if ((int64_t)p.layers * std::max({chunks, splits, levs, insts}) > 0x7fffffffLL)
+  if ((int64_t)p.layers * std::max(chunks, insts) > 0x7fffffffLL)
     return KVSEL_ERR_UNSUPPORTED;
-  const size_t o_seq = cv.take(seqs.size() * sizeof(JSeq));
+  const size_t o_tab = cv.take(jacap_table_bytes(jp));
   const size_t o_zk = cv.take(plane * sizeof(float2));
   const size_t o_w = cv.take(plane * sizeof(float));
   const size_t o_part = cv.take((size_t)p.layers * chunks * 2 * sizeof(float));
-  const size_t o_gram = cv.take((size_t)p.layers * splits * 128 * 128 * sizeof(float));
+  const size_t o_gram = cv.take(jp.segs.size() * 128 * 128 * sizeof(float));
   const size_t o_linv = cv.take((size_t)p.layers * insts * 2 * 128 * 128 * 2);
-  if ((e = cudaMemcpyAsync(ws + o_seq, seqs.data(), seqs.size() * sizeof(JSeq),
-                           cudaMemcpyHostToDevice, s)))
-    return cuda_fail(e, "cudaMemcpyAsync(jacap sequence table)");
+  // the tables, packed as jacap_table_bytes lays them out
+  std::vector<char> tab(jacap_table_bytes(jp), 0);
+  size_t o_segs = 0, o_cta = 0, o_inst = 0;
+  {
+    size_t at = 0;
+    auto put = [&](const void* src, size_t bytes) {
+      const size_t here = at;
+      if (bytes) std::memcpy(tab.data() + at, src, bytes);
+      at += (bytes + 15) & ~size_t(15);
+      return here;
+    };
+    put(seqs.data(), seqs.size() * sizeof(JSeq));
+    o_segs = put(jp.segs.data(), jp.segs.size() * sizeof(JSeg));
+    o_cta = put(jp.cta_seg.data(), jp.cta_seg.size() * sizeof(int32_t));
+    o_inst = put(jp.inst_seg.data(), jp.inst_seg.size() * sizeof(int32_t));
+  }
+  if ((e = cudaMemcpyAsync(ws + o_tab, tab.data(), tab.size(), cudaMemcpyHostToDevice, s)))
+    return cuda_fail(e, "cudaMemcpyAsync(jacap tables)");
   JacapArgs a{};
   a.q = q_win;
   a.k = K;
@@ -804,10 +851,12 @@ kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const vo
   a.S = p.S;
   a.T = p.T;
   a.n_scored = (int)seqs.size();
-  a.seqs = reinterpret_cast<const JSeq*>(ws + o_seq);
+  a.seqs = reinterpret_cast<const JSeq*>(ws + o_tab);
+  a.segs = reinterpret_cast<const JSeg*>(ws + o_tab + o_segs);
+  a.cta_seg = reinterpret_cast<const int32_t*>(ws + o_tab + o_cta);
+  a.inst_seg = reinterpret_cast<const int32_t*>(ws + o_tab + o_inst);
+  a.n_gram = (int)(jp.cta_seg.size() - 1);
   a.chunks_per_layer = chunks;
-  a.splits_per_layer = splits;
-  a.lev_per_layer = levs;
   a.inst_per_layer = insts;
   a.tau = tau;
   a.beta = beta;

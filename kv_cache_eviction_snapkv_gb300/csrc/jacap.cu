@@ -13,20 +13,26 @@
 // Four kernels per call, bf16 and d = 128 (the tensor-core operands):
 //   stats    one CTA per 512 prefix rows: the window statistics (recomputed by
 //            every CTA, W x d work), then z (base-2 units) and kappa per row
-//            (eight lanes per row, coalesced), and the chunk's max and sum of
-//            2^z. HBM-bound on K.
-//   gram     one CTA per range of 128-token tiles of an instance: merges the
-//            instance's softmax partials, computes w, scales each V tile by
-//            sqrt(w) and transposes it into a K-major, 128-byte-swizzled
-//            buffer (dimensions as rows, tokens as K), on which one tcgen05.mma
-//            with A = B = that buffer accumulates sum_t w_t v_t v_t^T (128 x 128,
-//            fp32, in TMEM); the partial is written out. HBM-bound on V.
-//   factor   one CTA per instance: A = I + the partials in a fixed order, the
-//            Cholesky factor and L^{-1} in fp32 shared memory, written as two
+//            (eight lanes per row, four rows per lane group in flight), and
+//            the chunk's max and sum of 2^z. HBM-bound on K.
+//   gram     persistent, at most one CTA per SM: the instances' 128-token tiles
+//            in instance order, cut into equal ranges, one per CTA; a range
+//            splits into pieces at instance boundaries. Per piece: merge the
+//            instance's softmax partials; per tile: w, then the V tile as TMA
+//            wrote it (128-byte swizzle, tokens as rows) scaled in place by
+//            sqrt(w) per token, on which tcgen05.mma with A = B = that tile read
+//            MN-major (dimensions as M and N, tokens as K) accumulates
+//            sum_t w_t v_t v_t^T (128 x 128, fp32, in TMEM, two accumulators
+//            taking pieces in turn); each piece's partial is written out.
+//            HBM-bound on V.
+//   factor   one CTA per instance: A = I + its pieces' partials in order, the
+//            Cholesky factor and L^{-1} in fp32 (8 x 8 register blocks, one
+//            column or row per step through shared memory), written as two
 //            bf16 matrices hi + lo (hi = bf16(L^{-1}), lo = bf16(L^{-1} - hi)).
-//   leverage one CTA per 8 tiles: y_t = L^{-1} v_t for 128 tokens at a time by
-//            tcgen05.mma (A = the V tile as loaded, B = L^{-1} hi, then lo,
-//            accumulated), r_t = w_t |y_t|^2 in the epilogue. HBM-bound on V.
+//   leverage persistent over the same pieces: L^{-1} (hi, lo) per piece, then
+//            y_t = L^{-1} v_t for 128 tokens at a time by tcgen05.mma (A = the
+//            V tile as loaded, B = hi, then lo, accumulated), r_t = w_t |y_t|^2
+//            in the epilogue. HBM-bound on V.
 // Every wait is bounded (KVSEL_ERR_TIMEOUT, then the roles drain and return).
 #include <cmath>
 #include <cstring>
@@ -64,6 +70,25 @@ __global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant_
   const int h = local / sq.n_chunks, c = local - h * sq.n_chunks;
   const int P = sq.len - a.W;
   const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  // K rows: each warp takes 16 consecutive rows a trip, each 8-lane group
+  // four of them (rows wb + 4u + grp), every load issued before any use; the
+  // first trip's loads go out before the window statistics
+  const int grp = lane >> 3, sub = lane & 7;
+  const int r_begin = c * kJChunk, r_end = min(P, r_begin + kJChunk);
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  uint4 kr[4][2];
+  auto load_trip = [&](int wb) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = min(wb + 4 * u + grp, r_end - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          kb + (((int64_t)layer * a.T + sq.tok_off + j) * a.H + h) * kJD + sub * 16);
+      kr[u][0] = __ldcs(src);
+      kr[u][1] = __ldcs(src + 1);
+    }
+  };
+  int wb = r_begin + warp * 16;
+  if (wb < r_end) load_trip(wb);
   {
     // the window statistics: rows staged 32 at a time with every thread
     // loading (16 bytes each), the recursion run by one thread per dimension
@@ -97,42 +122,41 @@ __global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant_
     }
   }
   __syncthreads();
-  const int grp = lane >> 3, sub = lane & 7;
   float mu[16], lam[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     mu[e] = mu_s[sub * 16 + e];
     lam[e] = lam_s[sub * 16 + e];
   }
-  const int r_begin = c * kJChunk, r_end = min(P, r_begin + kJChunk);
-  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sq.tok_off;
   float m = -INFINITY, l = 0.f;
-  for (int wb = r_begin + warp * 4; wb < r_end; wb += 32) {   // warp-uniform trips
-    const int row = wb + grp;
-    const int j = min(row, r_end - 1);
-    const uint4* src = reinterpret_cast<const uint4*>(
-        kb + (((int64_t)layer * a.T + sq.tok_off + j) * a.H + h) * kJD + sub * 16);
-    const uint4 k0 = __ldcs(src), k1 = __ldcs(src + 1);
-    const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-    float z = 0.f, kap = 0.f;
+  while (wb < r_end) {                                       // warp-uniform trips
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float kv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-      z = fmaf(mu[e], kv, z);
-      kap = fmaf(lam[e] * kv, kv, kap);
-    }
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[8] = {kr[u][0].x, kr[u][0].y, kr[u][0].z, kr[u][0].w,
+                             kr[u][1].x, kr[u][1].y, kr[u][1].z, kr[u][1].w};
+      float z = 0.f, kap = 0.f;
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      z += __shfl_xor_sync(0xffffffffu, z, off);
-      kap += __shfl_xor_sync(0xffffffffu, kap, off);
+      for (int e = 0; e < 16; ++e) {
+        const float kv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+        z = fmaf(mu[e], kv, z);
+        kap = fmaf(lam[e] * kv, kv, kap);
+      }
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) {
+        z += __shfl_xor_sync(0xffffffffu, z, off);
+        kap += __shfl_xor_sync(0xffffffffu, kap, off);
+      }
+      const int row = wb + 4 * u + grp;
+      if (row < r_end) {
+        if (sub == 0) a.zk[plane + row] = make_float2(z, kap);
+        const float mx = fmaxf(m, z);
+        l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + ex2(z - mx);
+        m = mx;
+      }
     }
-    if (row < r_end) {
-      if (sub == 0) a.zk[plane + row] = make_float2(z, kap);
-      const float mx = fmaxf(m, z);
-      l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + ex2(z - mx);
-      m = mx;
-    }
+    wb += 128;
+    if (wb < r_end) load_trip(wb);
   }
 #pragma unroll
   for (int off = 8; off <= 16; off <<= 1) {
@@ -162,20 +186,35 @@ __global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant_
 // gram
 // ---------------------------------------------------------------------------
 
-constexpr int kGStages = 3;                    // V tile ring
-constexpr int kGThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 transpose
-constexpr int kGWork = 256;                    // transposing threads
+constexpr int kGStages = 6;                    // V tile ring
+constexpr int kGThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 scale
+constexpr int kGWork = 256;                    // scaling threads
 
 struct GramSmem {
-  unsigned long long full[kGStages], empty[kGStages];
-  unsigned long long tfull[2], tempty[2];
-  unsigned long long done;
+  unsigned long long full[kGStages], empty[kGStages];   // V ring: loaded, free
+  unsigned long long scaled[kGStages];                  // V ring: scaled by sqrt(w)
+  unsigned long long done[2], tfree[2];                 // TMEM accumulators (one per piece)
   unsigned long long drain;                    // abort path: the MMA issuer's last commit
   uint32_t tmem_base;
   int abort_flag;
-  float norm_m, norm_s;                        // the instance's base-2 softmax max and sum
+  float norm_m, norm_s;                        // the piece's instance: base-2 softmax max and sum
   float sw[2][kJTile];                         // sqrt(w) of a tile's tokens (double buffer)
 };
+
+// The instance of a Gram piece: layer, sequence, head.
+struct JInst {
+  int layer, h;
+  const JSeq* sq;
+};
+
+__device__ __forceinline__ JInst jinst(const JacapArgs& a, int inst) {
+  JInst r;
+  r.layer = inst / a.inst_per_layer;
+  const int rem = inst - r.layer * a.inst_per_layer;
+  r.sq = &a.seqs[upper_find(a.n_scored, rem, [&](int i) { return a.seqs[i].inst_base; })];
+  r.h = rem - r.sq->inst_base;
+  return r;
+}
 
 struct GramParams {
   CUtensorMap tmv;                             // V as (D, H, layers * T)
@@ -186,7 +225,7 @@ __device__ __forceinline__ void work_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGWork) : "memory");
 }
 
-// Barrier of the transposing threads that also returns, in every one of them,
+// Barrier of the scaling threads that also returns, in every one of them,
 // whether any passed `v` true.
 __device__ __forceinline__ bool work_bar_any(bool v) {
   uint32_t r;
@@ -201,10 +240,18 @@ __device__ __forceinline__ bool work_bar_any(bool v) {
   return r != 0;
 }
 
-// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 64-column
-// swizzle atom (128-byte rows, 8-row swizzle period).
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Shared-memory descriptor of a V tile read MN-major (dimensions as M or N,
+// tokens as K), 128-byte swizzle as TMA wrote it: 64 dimensions per 128-byte
+// row, the next 64 in the other atom (leading byte offset 16 KiB), the next 8
+// tokens 1 KiB on (stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kAtom >> 4) << 16;   // LBO
+  d |= (uint64_t)(1024 >> 4) << 32;    // SBO
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
 }
 
 __global__ void __launch_bounds__(kGThreads, 1)
@@ -214,34 +261,22 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sv = smem;                                   // kGStages x 32 KiB
-  unsigned char* st = sv + kGStages * kJTileBytes;            // 2 x 32 KiB, transposed
-  GramSmem* ms = reinterpret_cast<GramSmem*>(st + 2 * kJTileBytes);
+  GramSmem* ms = reinterpret_cast<GramSmem*>(sv + kGStages * kJTileBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = a.wait_limit_ns;
   volatile int* abort_flag = &ms->abort_flag;
-
-  const int item = blockIdx.x;
-  const int layer = item / a.splits_per_layer;
-  const int rem = item - layer * a.splits_per_layer;
-  const JSeq& sq = a.seqs[find_jseq(a, rem, [&](int i) { return a.seqs[i].split_base; })];
-  const int local = rem - sq.split_base;
-  const int h = local / sq.n_split, s = local - h * sq.n_split;
-  const int P = sq.len - a.W;
-  const int n_tiles = (P + kJTile - 1) / kJTile;
-  const int per = (n_tiles + sq.n_split - 1) / sq.n_split;
-  const int t_begin = s * per, t_end = min(n_tiles, t_begin + per);
-  const int n_my = max(0, t_end - t_begin);
+  const int s_begin = a.cta_seg[blockIdx.x], s_end = a.cta_seg[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kGStages; ++i) {
       mbar_init(smem_u32(&ms->full[i]), 1);
       mbar_init(smem_u32(&ms->empty[i]), 1);
+      mbar_init(smem_u32(&ms->scaled[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&ms->tfull[b]), 1);
-      mbar_init(smem_u32(&ms->tempty[b]), 1);
+      mbar_init(smem_u32(&ms->done[b]), 1);
+      mbar_init(smem_u32(&ms->tfree[b]), 1);
     }
-    mbar_init(smem_u32(&ms->done), 1);
     mbar_init(smem_u32(&ms->drain), 1);
     ms->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -250,7 +285,7 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&ms->tmem_base)),
-                 "r"(kJD)
+                 "r"(2 * kJD)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -262,178 +297,203 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
   bool mma_issued = false;
 
   if (warp == 0) {
+    // ---- TMA producer: the V tiles of every piece, in order
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
-      for (int i = 0; i < n_my; ++i) {
-        if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
-          *abort_flag = 1;
-          record_status(a.status, KVSEL_ERR_TIMEOUT);
-          break;
-        }
-        const uint32_t bar = smem_u32(&ms->full[stage]);
-        mbar_expect_tx(bar, kJTileBytes);
-        const int row = (int)((int64_t)layer * a.T + sq.tok_off + (t_begin + i) * kJTile);
+      bool ok = true;
+      for (int sg = s_begin; ok && sg < s_end; ++sg) {
+        const JSeg pc = a.segs[sg];
+        const JInst in = jinst(a, pc.inst);
+        const int64_t row0 = (int64_t)in.layer * a.T + in.sq->tok_off;
+        for (int t = pc.t_begin; t < pc.t_end; ++t) {
+          if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
+            *abort_flag = 1;
+            record_status(a.status, KVSEL_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&ms->full[stage]);
+          mbar_expect_tx(bar, kJTileBytes);
+          const int row = (int)(row0 + (int64_t)t * kJTile);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem_u32(sv + stage * kJTileBytes + hf * kAtom), &G.tmv, bar, hf * 64, h,
-                      row, pol);
-        armed |= 1u << stage;
-        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == kGStages) {
-          stage = 0;
-          phase ^= 1;
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem_u32(sv + stage * kJTileBytes + hf * kAtom), &G.tmv, bar, hf * 64, in.h,
+                        row, pol);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
     }
   } else if (warp == 1) {
+    // ---- MMA issuer: piece k accumulates into TMEM columns (k % 2) * 128 ..
     if (lane == 0) {
-      constexpr uint32_t kIdesc = instr_desc(kJD, kJD);
-      const uint32_t st_addr = smem_u32(st);
+      constexpr uint32_t kIdesc = instr_desc(kJD, kJD) | (1u << 15) | (1u << 16);  // A, B MN-major
+      const uint32_t sv_addr = smem_u32(sv);
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
-      for (int i = 0; ok && i < n_my; ++i) {
-        const int b = i & 1;
-        if (!mbar_wait(smem_u32(&ms->tfull[b]), (uint32_t)(i >> 1) & 1, limit, abort_flag)) {
+      for (int k = 0; ok && k < s_end - s_begin; ++k) {
+        const JSeg pc = a.segs[s_begin + k];
+        const int ab = k & 1;
+        if (!mbar_wait(smem_u32(&ms->tfree[ab]), ((uint32_t)(k >> 1) & 1) ^ 1, limit, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(ab * kJD);
+        for (int t = pc.t_begin; t < pc.t_end; ++t) {
+          if (!mbar_wait(smem_u32(&ms->scaled[stage]), phase, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kJTile / 16; ++kk) {
-          const uint32_t addr = st_addr + b * kJTileBytes + (kk >> 2) * kAtom + (kk & 3) * 32;
-          tc_mma(tmem_base, smem_desc(addr), smem_desc(addr), kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kJTile / 16; ++kk) {          // 16 tokens (2 KiB of rows) each
+            const uint32_t addr = sv_addr + stage * kJTileBytes + kk * 2048;
+            tc_mma(d_tmem, smem_desc_mn(addr), smem_desc_mn(addr), kIdesc,
+                   (t > pc.t_begin || kk > 0) ? 1u : 0u);
+          }
+          mma_issued = true;
+          tc_commit(smem_u32(&ms->empty[stage]));
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        mma_issued = true;
-        tc_commit(smem_u32(&ms->tempty[b]));
+        if (ok) tc_commit(smem_u32(&ms->done[ab]));
       }
-      if (ok) {
-        tc_commit(smem_u32(&ms->done));
-      } else {
+      if (!ok) {
         *abort_flag = 1;
         record_status(a.status, KVSEL_ERR_TIMEOUT);
       }
     }
   } else {
-    // ---- transposers (warps 2..9): softmax normaliser, w, sqrt(w) V^T tiles
+    // ---- scaling warps (2..9): per piece the instance's softmax normaliser,
+    // then per tile w and the tile scaled by sqrt(w); at the end of the piece
+    // its partial Gram out of TMEM
     const int tid = threadIdx.x - 64;
-    if (warp == 2) {
-      // merge the instance's statistics partials in a fixed order
-      const float* pr = a.part + 2 * ((int64_t)layer * a.chunks_per_layer + sq.chunk_base +
-                                      (int64_t)h * sq.n_chunks);
-      float mx = -INFINITY;
-      for (int c = lane; c < sq.n_chunks; c += 32) mx = fmaxf(mx, pr[2 * c]);
-      for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      float sum = 0.f;
-      for (int c = lane; c < sq.n_chunks; c += 32) sum = fmaf(pr[2 * c + 1], ex2(pr[2 * c] - mx), sum);
-      for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) {
-        ms->norm_m = mx;
-        ms->norm_s = sum;
-      }
-    }
-    work_bar();
-    const float nm = ms->norm_m, inv_s = 1.f / ms->norm_s;
-    const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sq.tok_off;
-    // sqrt(w) of a tile's tokens into sw[buf] (threads 0..127, one token each)
-    auto weights_of = [&](int tile, int buf) {
-      if (tid < kJTile) {
-        const int t = tile * kJTile + tid;
-        float w = 0.f;
-        if (t < P) {
-          const float2 zk = a.zk[plane + t];
-          const float al = ex2(zk.x - nm) * inv_s;
-          const float g = al * (1.f - al);
-          w = g * g * zk.y * (1.f / kJD);
-          a.wts[plane + t] = w;
-        }
-        ms->sw[buf][tid] = sqrtf(w);
-      }
-    };
-    if (n_my > 0) weights_of(t_begin, 0);
-    work_bar();
-    // transposition by 8 x 8 blocks: warp wq takes dimension blocks 2wq, 2wq+1
-    // and, per step, token blocks 2p, 2p+1 (four blocks: one ldmatrix.x4.trans
-    // from the V tile, one stmatrix.x4 into the transposed buffer; each 8-row
-    // phase of either touches eight distinct chunks of a swizzle period)
     const int wq = tid >> 5, lid = tid & 31;
-    const int m_of = lid >> 3, r_of = lid & 7;          // the matrix and row this lane addresses
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int i = 0; i < n_my; ++i) {
-      const int b = i & 1;
-      if (i + 1 < n_my) weights_of(t_begin + i + 1, (i + 1) & 1);
-      bool mine = mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag);
-      if (mine && i >= 2)
-        mine = mbar_wait(smem_u32(&ms->tempty[b]), (uint32_t)((i - 2) >> 1) & 1, limit, abort_flag);
-      if (mine) {
-        const uint32_t vt = smem_u32(sv + stage * kJTileBytes);
-        const uint32_t tt = smem_u32(st + b * kJTileBytes);
-        const float* sw = ms->sw[i & 1];
-#pragma unroll 2
-        for (int pstep = 0; pstep < 8; ++pstep) {
-          // this lane's address: matrix m_of = (token block 2p + m/2, dimension block 2wq + m%2)
-          const int tbl = 2 * pstep + (m_of >> 1), dbl = 2 * wq + (m_of & 1);
-          const uint32_t src = vt + (dbl >> 3) * kAtom + swz(tbl * 8 + r_of, dbl & 7);
-          uint32_t rg[4];
-          asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(rg[0]), "=r"(rg[1]), "=r"(rg[2]), "=r"(rg[3])
-                       : "r"(src)
-                       : "memory");
-          // register m holds, for dimension dbl*8 + lid/4, tokens (lid%4)*2 and +1 of
-          // token block 2p + m/2: scale each by its sqrt(w)
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int t0 = (2 * pstep + (m >> 1)) * 8 + (lid & 3) * 2;
-            const float f0 = sw[t0], f1 = sw[t0 + 1];
-            const float x0 = __uint_as_float(rg[m] << 16), x1 = __uint_as_float(rg[m] & 0xFFFF0000u);
-            const __nv_bfloat162 p2 = __floats2bfloat162_rn(f0 != 0.f ? f0 * x0 : 0.f,
-                                                            f1 != 0.f ? f1 * x1 : 0.f);
-            rg[m] = *reinterpret_cast<const uint32_t*>(&p2);
-          }
-          // stored matrix m_of: rows = dimensions dbl*8 .., 8 tokens of block tbl
-          const uint32_t dst = tt + (tbl >> 3) * kAtom + swz(dbl * 8 + r_of, tbl & 7);
-          asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst),
-                       "r"(rg[0]), "r"(rg[1]), "r"(rg[2]), "r"(rg[3])
-                       : "memory");
+    int i = 0;                                          // tiles so far
+    for (int k = 0; ok && k < s_end - s_begin; ++k) {
+      const int sg = s_begin + k;
+      const JSeg pc = a.segs[sg];
+      const JInst in = jinst(a, pc.inst);
+      const JSeq& sq = *in.sq;
+      const int P = sq.len - a.W;
+      const int64_t plane = ((int64_t)in.layer * a.H + in.h) * a.T + sq.tok_off;
+      if (wq == 0) {
+        // merge the instance's statistics partials in a fixed order
+        const float* pr = a.part + 2 * ((int64_t)in.layer * a.chunks_per_layer + sq.chunk_base +
+                                        (int64_t)in.h * sq.n_chunks);
+        float mx = -INFINITY;
+        for (int c = lid; c < sq.n_chunks; c += 32) mx = fmaxf(mx, pr[2 * c]);
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float sum = 0.f;
+        for (int c = lid; c < sq.n_chunks; c += 32) sum = fmaf(pr[2 * c + 1], ex2(pr[2 * c] - mx), sum);
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lid == 0) {
+          ms->norm_m = mx;
+          ms->norm_s = sum;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      // the tile written by all, or a wait given up somewhere (same answer everywhere)
+      work_bar();
+      const float nm = ms->norm_m, inv_s = 1.f / ms->norm_s;
+      // (z, kappa) of token tid of a tile (threads 0..127), loaded two tiles
+      // ahead of its use; then w and sqrt(w) into sw[buf]
+      auto fetch = [&](int tile) {
+        const int t = tile * kJTile + tid;
+        return (tid < kJTile && tile < pc.t_end && t < P) ? a.zk[plane + t] : make_float2(0.f, -1.f);
+      };
+      auto weigh = [&](int tile, int buf, float2 zk) {
+        if (tid < kJTile) {
+          float w = 0.f;
+          if (zk.y >= 0.f) {                  // a prefix token (kappa >= 0)
+            const float al = ex2(zk.x - nm) * inv_s;
+            const float g = al * (1.f - al);
+            w = g * g * zk.y * (1.f / kJD);
+            a.wts[plane + tile * kJTile + tid] = w;
+          }
+          ms->sw[buf][tid] = sqrtf(w);
+        }
+      };
+      float2 z1 = fetch(pc.t_begin + 1), z2 = fetch(pc.t_begin + 2);
+      weigh(pc.t_begin, i & 1, fetch(pc.t_begin));
+      work_bar();
+      // scaling in place: thread tid takes the 16-byte chunks tid + 256 j of
+      // the tile (row (chunk / 8) % 128 of atom chunk / 1024; the swizzle only
+      // permutes chunks within a row)
+      for (int t = pc.t_begin; t < pc.t_end; ++t, ++i) {
+        if (t + 1 < pc.t_end) weigh(t + 1, (i + 1) & 1, z1);
+        z1 = z2;
+        z2 = fetch(t + 3);
+        const bool mine = mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag);
+        if (mine) {
+          unsigned char* vt = sv + stage * kJTileBytes;
+          const float* sw = ms->sw[i & 1];
+#pragma unroll
+          for (int j = 0; j < kJTileBytes / 16 / kGWork; ++j) {
+            const int e = tid + kGWork * j;
+            const float f = sw[(e >> 3) & (kJTile - 1)];
+            uint4* p = reinterpret_cast<uint4*>(vt + e * 16);
+            uint4 x = *p;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
+              const __nv_bfloat162 p2 = __floats2bfloat162_rn(f * x0, f * x1);
+              w[q] = f != 0.f ? *reinterpret_cast<const uint32_t*>(&p2) : 0u;
+            }
+            *p = x;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        // the tile scaled by all, or a wait given up somewhere (same answer everywhere)
+        if (work_bar_any(!mine)) {
+          ok = false;
+          break;
+        }
+        if (tid == 0) mbar_arrive(smem_u32(&ms->scaled[stage]));
+        if (++stage == kGStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      // the piece's partial: TMEM lanes are dimensions d1, columns d2; warp
+      // w reads lane quarter w % 4 and column half (w - 2) / 4
+      const int ab = k & 1;
+      const bool mine = mbar_wait(smem_u32(&ms->done[ab]), (uint32_t)(k >> 1) & 1, limit, abort_flag);
       if (work_bar_any(!mine)) {
         ok = false;
         break;
       }
-      if (tid == 0) {
-        mbar_arrive(smem_u32(&ms->tfull[b]));
-        mbar_arrive(smem_u32(&ms->empty[stage]));
-      }
-      if (++stage == kGStages) {
-        stage = 0;
-        phase ^= 1;
-      }
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      record_status(a.status, KVSEL_ERR_TIMEOUT);
-    } else if (n_my > 0 &&
-               mbar_wait(smem_u32(&ms->done), 0, limit, abort_flag)) {
-      // epilogue: TMEM lanes are dimensions d1, columns d2; warp w reads lane
-      // quarter w % 4 and column half (w - 2) / 4
       tc_fence_after();
       const int quarter = warp & 3, half = (warp - 2) >> 2;
       const int d1 = quarter * 32 + lane;
-      float* out = a.gram + ((int64_t)item * kJD + d1) * kJD + half * 64;
+      float* out = a.gram + ((int64_t)sg * kJD + d1) * kJD + half * 64;
 #pragma unroll
       for (int cblk = 0; cblk < 64; cblk += 32) {
         float v[32];
-        tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + half * 64 + cblk, v);
+        tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kJD + half * 64 + cblk,
+                           v);
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(out + cblk + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       }
-    } else if (n_my > 0) {
+      tc_fence_before();
+      work_bar();
+      if (tid == 0) mbar_arrive(smem_u32(&ms->tfree[ab]));
+    }
+    if (!ok) {
       *abort_flag = 1;
       record_status(a.status, KVSEL_ERR_TIMEOUT);
     }
@@ -456,7 +516,7 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kJD)
+                 "r"(2 * kJD)
                  : "memory");
   }
 }
@@ -465,100 +525,159 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
 // factor: A = I + sum of the partial Grams, Cholesky, L^{-1} as bf16 hi + lo
 // ---------------------------------------------------------------------------
 
-constexpr int kFLd = kJD + 1;                  // padded row of the fp32 matrices
+constexpr int kFB = kJD / 8;                   // 8 x 8 blocks per side
 
+// One CTA per instance, 256 threads; thread (bi, bk) = (tid / 16, tid % 16)
+// holds block (bi, bk) of the matrix in registers (the lower blocks bk <= bi
+// take part). Both phases are right-looking, one column (row) per step and
+// one barrier per step:
+//   Cholesky  step j: the owners of column j (bk = j / 8) store its current
+//             values to shared memory; every thread reads the pivot d = A[j][j]
+//             and the column, l_i = A[i][j] / sqrt(d), and updates its
+//             entries right of j by -l_i l_k. The stored columns (before
+//             scaling) and 1 / sqrt(d) are kept for the inverse.
+//   inverse   L X = I by rows: B = I; step j: X[j][:] = B[j][:] / L[j][j]
+//             (the owners of row j, bi = j / 8, scale it and store it to a
+//             double-buffered row), then every row i > j takes
+//             B[i][:] -= L[i][j] X[j][:].
+// Entries above the diagonal of a diagonal block collect values that are
+// never read; the output writes zeros there.
 __global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
-  extern __shared__ float fs[];
-  float* A = fs;                               // [kJD][kFLd]: A, then L in the lower triangle
-  float* X = fs + kJD * kFLd;                  // L^{-1} (lower triangle)
+  extern __shared__ float4 fs4[];
+  float* Lc = reinterpret_cast<float*>(fs4);    // [kJD][kJD]: column j of the updated matrix at step j
+  __shared__ float dinv[kJD];                   // 1 / L[j][j]
+  __shared__ __align__(16) float xrow[2][kJD];  // X[j][:] of the current inverse step
   __shared__ int bad;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, bi = tid >> 4, bk = tid & (kFB - 1);
+  const bool act = bk <= bi;
   const int inst = blockIdx.x;
-  const int layer = inst / a.inst_per_layer;
-  const int rem = inst - layer * a.inst_per_layer;
-  const JSeq& sq = a.seqs[find_jseq(a, rem, [&](int i) { return a.seqs[i].inst_base; })];
-  const int h = rem - sq.inst_base;
-  const int64_t g0 = (int64_t)layer * a.splits_per_layer + sq.split_base + (int64_t)h * sq.n_split;
+  const int s_lo = a.inst_seg[inst], n_part = a.inst_seg[inst + 1] - s_lo;
   if (tid == 0) bad = 0;
-  // A = I + the partial Grams (fixed order), lower triangle
-  {
-    const float* __restrict__ gp = a.gram + g0 * kJD * kJD;
-    constexpr int kPer = kJD * kJD / 256;       // elements per thread (every 256th)
-    float acc[kPer];
+
+  float R[8][8];
+  auto set_identity = [&]() {
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * 256;
-      acc[q] = (e >> 7) == (e & (kJD - 1)) ? 1.f : 0.f;
-    }
-    const int nsp = sq.n_split;
-    for (int sp = 0; sp < nsp; ++sp) {         // every load of a partial in flight at once
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) acc[q] += __ldg(gp + (int64_t)sp * kJD * kJD + tid + q * 256);
-    }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * 256, i = e >> 7, j = e & (kJD - 1);
-      if (j <= i) A[i * kFLd + j] = acc[q];
-    }
-  }
-  __syncthreads();
-  // two threads per row (or column) of each step, each taking every other k
-  // of the dot product with four accumulators; the halves are added by a
-  // shuffle
-  const int pair = tid >> 1, half = tid & 1;
-  auto dot = [&](const float* x, int xs, const float* y, int ys, int k0, int k1) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int k = k0 + half;
-    for (; k + 6 < k1; k += 8) {
-      s0 = fmaf(x[k * xs], y[k * ys], s0);
-      s1 = fmaf(x[(k + 2) * xs], y[(k + 2) * ys], s1);
-      s2 = fmaf(x[(k + 4) * xs], y[(k + 4) * ys], s2);
-      s3 = fmaf(x[(k + 6) * xs], y[(k + 6) * ys], s3);
-    }
-    for (; k < k1; k += 2) s0 = fmaf(x[k * xs], y[k * ys], s0);
-    float acc = (s0 + s1) + (s2 + s3);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    return acc;
+      for (int c = 0; c < 8; ++c) R[r][c] = (bi == bk && r == c) ? 1.f : 0.f;
   };
-  // Cholesky, left-looking, one column at a time: L[j][j] = sqrt(A[j][j] -
-  // sum_k L[j][k]^2), then L[i][j] = (A[i][j] - sum_{k<j} L[i][k] L[j][k]) /
-  // L[j][j] for the rows below
-  for (int j = 0; j < kJD; ++j) {
-    if (tid < 32) {                            // the diagonal: one warp, a strided dot product
-      float acc = 0.f;
-      for (int k = tid; k < j; k += 32) acc = fmaf(A[j * kFLd + k], A[j * kFLd + k], acc);
-      for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (tid == 0) {
-        const float p = A[j * kFLd + j] - acc;
-        if (!(p > 0.f) || !finite_f(p)) bad = 1;
-        A[j * kFLd + j] = sqrtf(fmaxf(p, 1e-30f));
+  // A = I + the partial Grams, in a fixed order
+  set_identity();
+  if (act) {
+    const float* __restrict__ gp = a.gram + (int64_t)s_lo * kJD * kJD + (bi * 8) * kJD + bk * 8;
+    for (int sp = 0; sp < n_part; ++sp) {
+      const float4* src = reinterpret_cast<const float4*>(gp + (int64_t)sp * kJD * kJD);
+      float4 x[16];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        x[2 * r] = __ldg(src + r * (kJD / 4));
+        x[2 * r + 1] = __ldg(src + r * (kJD / 4) + 1);
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        R[r][0] += x[2 * r].x, R[r][1] += x[2 * r].y, R[r][2] += x[2 * r].z, R[r][3] += x[2 * r].w;
+        R[r][4] += x[2 * r + 1].x, R[r][5] += x[2 * r + 1].y, R[r][6] += x[2 * r + 1].z;
+        R[r][7] += x[2 * r + 1].w;
       }
     }
-    __syncthreads();
-    const float inv = 1.f / A[j * kFLd + j];
-    const int i = j + 1 + pair;                // rows j+1 .. 127 (pairs of threads)
-    const float acc = dot(A + (i < kJD ? i : j) * kFLd, 1, A + j * kFLd, 1, 0, j);
-    if (i < kJD && half == 0) A[i * kFLd + j] = (A[i * kFLd + j] - acc) * inv;
-    __syncthreads();
   }
-  // X = L^{-1}, one row at a time: X[i][i] = 1 / L[i][i] and, for c < i,
-  // X[i][c] = -(sum_{k=c}^{i-1} L[i][k] X[k][c]) / L[i][i], a column per pair
-  for (int i = 0; i < kJD; ++i) {
-    const float inv = 1.f / A[i * kFLd + i];
-    const int c = pair;                        // columns 0 .. 127
-    const float acc = dot(A + i * kFLd, 1, X + c, kFLd, c, c <= i ? i : c);
-    if (c <= i && half == 0) X[i * kFLd + c] = c == i ? inv : -acc * inv;
-    __syncthreads();
+  auto load8 = [](const float* p, float* v, float s) {
+    const float4 u0 = reinterpret_cast<const float4*>(p)[0], u1 = reinterpret_cast<const float4*>(p)[1];
+    v[0] = u0.x * s, v[1] = u0.y * s, v[2] = u0.z * s, v[3] = u0.w * s;
+    v[4] = u1.x * s, v[5] = u1.y * s, v[6] = u1.z * s, v[7] = u1.w * s;
+  };
+
+  // ---- Cholesky
+  for (int jb = 0; jb < kFB; ++jb) {
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = jb * 8 + jj;
+      if (bk == jb && bi >= jb) {
+        float4* dst = reinterpret_cast<float4*>(Lc + j * kJD + bi * 8);
+        dst[0] = make_float4(R[0][jj], R[1][jj], R[2][jj], R[3][jj]);
+        dst[1] = make_float4(R[4][jj], R[5][jj], R[6][jj], R[7][jj]);
+      }
+      __syncthreads();
+      const float d = Lc[j * kJD + j];
+      const float inv = 1.f / sqrtf(fmaxf(d, 1e-30f));
+      if (tid == 0) {
+        dinv[j] = inv;
+        if (!(d > 0.f) || !finite_f(d)) bad = 1;
+      }
+      if (act && bk >= jb) {
+        float lr[8], lc[8];
+        load8(Lc + j * kJD + bi * 8, lr, inv);
+        load8(Lc + j * kJD + bk * 8, lc, inv);
+        if (bk == jb) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = jj + 1; c < 8; ++c) R[r][c] = fmaf(-lr[r], lc[c], R[r][c]);
+        } else {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-lr[r], lc[c], R[r][c]);
+        }
+      }
+    }
   }
+
+  // ---- X = L^{-1}
+  set_identity();
+  for (int jb = 0; jb < kFB; ++jb) {
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = jb * 8 + jj;
+      float* xr = xrow[jj & 1];
+      if (bi == jb && bk <= jb) {
+        const float di = dinv[j];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) R[jj][c] *= di;
+        float4* dst = reinterpret_cast<float4*>(xr + bk * 8);
+        dst[0] = make_float4(R[jj][0], R[jj][1], R[jj][2], R[jj][3]);
+        dst[1] = make_float4(R[jj][4], R[jj][5], R[jj][6], R[jj][7]);
+      }
+      __syncthreads();
+      if (bi >= jb && bk <= jb) {
+        float li[8], x[8];
+        load8(Lc + j * kJD + bi * 8, li, dinv[j]);
+        load8(xr + bk * 8, x, 1.f);
+        if (bi == jb) {
+#pragma unroll
+          for (int r = jj + 1; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-li[r], x[c], R[r][c]);
+        } else {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-li[r], x[c], R[r][c]);
+        }
+      }
+    }
+  }
+
+  // ---- output: rows bi*8 .. of L^{-1}, columns bk*8 .., as bf16 hi and lo
   __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(a.linv) + (int64_t)inst * 2 * kJD * kJD;
   __nv_bfloat16* lo = hi + kJD * kJD;
-  for (int e = tid; e < kJD * kJD; e += blockDim.x) {
-    const int r = e >> 7, c = e & (kJD - 1);
-    const float x = c <= r ? X[r * kFLd + c] : 0.f;
-    const __nv_bfloat16 xh = __float2bfloat16_rn(x);
-    hi[e] = xh;
-    lo[e] = __float2bfloat16_rn(x - __bfloat162float(xh));
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int c = 0; c < 8; c += 2) {
+      const float x0 = (bk < bi || (bk == bi && c <= r)) ? R[r][c] : 0.f;
+      const float x1 = (bk < bi || (bk == bi && c + 1 <= r)) ? R[r][c + 1] : 0.f;
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - __low2float(h2), x1 - __high2float(h2));
+      ph[c >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+      pl[c >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+    }
+    const int64_t off = (int64_t)(bi * 8 + r) * kJD + bk * 8;
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
+  __syncthreads();
   if (tid == 0 && bad) record_status(a.status, KVSEL_ERR_NONFINITE);
 }
 
@@ -572,7 +691,7 @@ constexpr int kLBufs = 4;                      // TMEM accumulators of 128 colum
 
 struct LevSmem {
   unsigned long long full[kLStages], empty[kLStages];
-  unsigned long long lfull;
+  unsigned long long lfull, lfree;             // L^{-1} of the current piece; its last MMA done
   unsigned long long ready[kLBufs], tfree[kLBufs];
   unsigned long long drain;                    // abort path: the MMA issuer's last commit
   uint32_t tmem_base;
@@ -585,6 +704,10 @@ struct LevParams {
   JacapArgs a;
 };
 
+// Persistent over the Gram kernel's pieces (the same CTA ranges): per piece,
+// L^{-1} (hi, lo) is loaded once the previous piece's MMAs are done, then
+// its V tiles stream through the ring; the tile count, the ring and the four
+// TMEM accumulators run on across pieces.
 __global__ void __launch_bounds__(kLThreads, 1)
 jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
   const JacapArgs& a = Lp.a;
@@ -597,18 +720,7 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long limit = a.wait_limit_ns;
   volatile int* abort_flag = &ms->abort_flag;
-
-  const int item = blockIdx.x;
-  const int layer = item / a.lev_per_layer;
-  const int rem = item - layer * a.lev_per_layer;
-  const JSeq& sq = a.seqs[find_jseq(a, rem, [&](int i) { return a.seqs[i].lev_base; })];
-  const int local = rem - sq.lev_base;
-  const int h = local / sq.n_lev, g = local - h * sq.n_lev;
-  const int P = sq.len - a.W;
-  const int n_tiles = (P + kJTile - 1) / kJTile;
-  const int t_begin = g * kJLevTiles, t_end = min(n_tiles, t_begin + kJLevTiles);
-  const int n_my = max(0, t_end - t_begin);
-  const int inst = layer * a.inst_per_layer + sq.inst_base + h;
+  const int s_begin = a.cta_seg[blockIdx.x], s_end = a.cta_seg[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLStages; ++i) {
@@ -616,6 +728,7 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
       mbar_init(smem_u32(&ms->empty[i]), 1);
     }
     mbar_init(smem_u32(&ms->lfull), 1);
+    mbar_init(smem_u32(&ms->lfree), 1);
     for (int b = 0; b < kLBufs; ++b) {
       mbar_init(smem_u32(&ms->ready[b]), 1);
       mbar_init(smem_u32(&ms->tfree[b]), 4);
@@ -637,76 +750,102 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
   tc_fence_after();
   const uint32_t tmem_base = ms->tmem_base;
   uint32_t armed = 0, armed_par = 0;
-  bool l_armed = false, mma_issued = false;
+  int l_loads = 0;                             // L^{-1} loads issued (lfull phases armed)
+  bool mma_issued = false;
 
   if (warp == 0) {
-    if (lane == 0 && n_my > 0) {
+    // ---- TMA producer
+    if (lane == 0) {
       const uint64_t pol_v = policy_evict_first(), pol_l = policy_evict_last();
-      const uint32_t lbar = smem_u32(&ms->lfull);
-      mbar_expect_tx(lbar, 2 * kJTileBytes);
-#pragma unroll
-      for (int which = 0; which < 2; ++which)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem_u32(sl + which * kJTileBytes + hf * kAtom), &Lp.tml, lbar, hf * 64, 0,
-                      inst * 2 + which, pol_l);
-      l_armed = true;
       int stage = 0;
       uint32_t phase = 0;
-      for (int i = 0; i < n_my; ++i) {
-        if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
-          *abort_flag = 1;
-          record_status(a.status, KVSEL_ERR_TIMEOUT);
-          break;
-        }
-        const uint32_t bar = smem_u32(&ms->full[stage]);
-        mbar_expect_tx(bar, kJTileBytes);
-        const int row = (int)((int64_t)layer * a.T + sq.tok_off + (t_begin + i) * kJTile);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem_u32(sv + stage * kJTileBytes + hf * kAtom), &Lp.tmv, bar, hf * 64, h,
-                      row, pol_v);
-        armed |= 1u << stage;
-        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == kLStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && n_my > 0) {
-      constexpr uint32_t kIdesc = instr_desc(kJD, kJTile);
-      const uint32_t sv_addr = smem_u32(sv), sl_addr = smem_u32(sl);
-      bool ok = mbar_wait(smem_u32(&ms->lfull), 0, limit, abort_flag);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int i = 0; ok && i < n_my; ++i) {
-        const int b = i % kLBufs;
-        if (!mbar_wait(smem_u32(&ms->tfree[b]), ((uint32_t)(i / kLBufs) & 1) ^ 1, limit,
-                       abort_flag) ||
-            !mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag)) {
+      bool ok = true;
+      for (int k = 0; ok && k < s_end - s_begin; ++k) {
+        const JSeg pc = a.segs[s_begin + k];
+        const JInst in = jinst(a, pc.inst);
+        // L^{-1} of this piece's instance, once the last piece's MMAs read theirs
+        if (!mbar_wait(smem_u32(&ms->lfree), ((uint32_t)k & 1) ^ 1, limit, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(b * kJD);
+        const uint32_t lbar = smem_u32(&ms->lfull);
+        mbar_expect_tx(lbar, 2 * kJTileBytes);
 #pragma unroll
         for (int which = 0; which < 2; ++which)
 #pragma unroll
-          for (int kk = 0; kk < kJD / 16; ++kk) {
-            const uint32_t a_addr = sv_addr + stage * kJTileBytes + (kk >> 2) * kAtom + (kk & 3) * 32;
-            const uint32_t b_addr = sl_addr + which * kJTileBytes + (kk >> 2) * kAtom + (kk & 3) * 32;
-            tc_mma(d_tmem, smem_desc(a_addr), smem_desc(b_addr), kIdesc,
-                   (which > 0 || kk > 0) ? 1u : 0u);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem_u32(sl + which * kJTileBytes + hf * kAtom), &Lp.tml, lbar, hf * 64, 0,
+                        pc.inst * 2 + which, pol_l);
+        ++l_loads;
+        const int64_t row0 = (int64_t)in.layer * a.T + in.sq->tok_off;
+        for (int t = pc.t_begin; t < pc.t_end; ++t) {
+          if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
+            ok = false;
+            break;
           }
-        mma_issued = true;
-        tc_commit(smem_u32(&ms->empty[stage]));
-        tc_commit(smem_u32(&ms->ready[b]));
-        if (++stage == kLStages) {
-          stage = 0;
-          phase ^= 1;
+          const uint32_t bar = smem_u32(&ms->full[stage]);
+          mbar_expect_tx(bar, kJTileBytes);
+          const int row = (int)(row0 + (int64_t)t * kJTile);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem_u32(sv + stage * kJTileBytes + hf * kAtom), &Lp.tmv, bar, hf * 64,
+                        in.h, row, pol_v);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kLStages) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(a.status, KVSEL_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: y = L^{-1} v for 128 tokens, hi then lo, into TMEM buffer i % 4
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = instr_desc(kJD, kJTile);
+      const uint32_t sv_addr = smem_u32(sv), sl_addr = smem_u32(sl);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int i = 0;
+      for (int k = 0; ok && k < s_end - s_begin; ++k) {
+        const JSeg pc = a.segs[s_begin + k];
+        if (!mbar_wait(smem_u32(&ms->lfull), (uint32_t)k & 1, limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        for (int t = pc.t_begin; t < pc.t_end; ++t, ++i) {
+          const int b = i % kLBufs;
+          if (!mbar_wait(smem_u32(&ms->tfree[b]), ((uint32_t)(i / kLBufs) & 1) ^ 1, limit,
+                         abort_flag) ||
+              !mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * kJD);
+#pragma unroll
+          for (int which = 0; which < 2; ++which)
+#pragma unroll
+            for (int kk = 0; kk < kJD / 16; ++kk) {
+              const uint32_t a_addr = sv_addr + stage * kJTileBytes + (kk >> 2) * kAtom + (kk & 3) * 32;
+              const uint32_t b_addr = sl_addr + which * kJTileBytes + (kk >> 2) * kAtom + (kk & 3) * 32;
+              tc_mma(d_tmem, smem_desc(a_addr), smem_desc(b_addr), kIdesc,
+                     (which > 0 || kk > 0) ? 1u : 0u);
+            }
+          mma_issued = true;
+          tc_commit(smem_u32(&ms->empty[stage]));
+          tc_commit(smem_u32(&ms->ready[b]));
+          if (++stage == kLStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) tc_commit(smem_u32(&ms->lfree));
       }
       if (!ok) {
         *abort_flag = 1;
@@ -716,28 +855,34 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
   } else {
     // ---- epilogue (warps 2..5): lane quarter warp % 4, one token per lane
     const int quarter = warp & 3;
-    const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sq.tok_off;
     bool ok = true;
-    for (int i = 0; ok && i < n_my; ++i) {
-      const int b = i % kLBufs;
-      const int t = (t_begin + i) * kJTile + quarter * 32 + lane;
-      const float w = t < P ? a.wts[plane + t] : 0.f;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->ready[b]), (uint32_t)(i / kLBufs) & 1,
-                                               limit, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      float ss = 0.f;
+    int i = 0;
+    for (int k = 0; ok && k < s_end - s_begin; ++k) {
+      const JSeg pc = a.segs[s_begin + k];
+      const JInst in = jinst(a, pc.inst);
+      const int P = in.sq->len - a.W;
+      const int64_t plane = ((int64_t)in.layer * a.H + in.h) * a.T + in.sq->tok_off;
+      for (int tl = pc.t_begin; tl < pc.t_end; ++tl, ++i) {
+        const int b = i % kLBufs;
+        const int t = tl * kJTile + quarter * 32 + lane;
+        const float w = t < P ? a.wts[plane + t] : 0.f;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->ready[b]), (uint32_t)(i / kLBufs) & 1,
+                                                 limit, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        float ss = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kJD; c0 += 32) {
-        float y[32];
-        tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + b * kJD + c0, y);
+        for (int c0 = 0; c0 < kJD; c0 += 32) {
+          float y[32];
+          tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + b * kJD + c0, y);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ss = fmaf(y[e], y[e], ss);
+          for (int e = 0; e < 32; ++e) ss = fmaf(y[e], y[e], ss);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ms->tfree[b]));
+        if (t < P) a.scores[plane + t] = w * ss;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ms->tfree[b]));
-      if (t < P) a.scores[plane + t] = w * ss;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -749,7 +894,7 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
   __syncthreads();
   if (ms->abort_flag) {
     if (warp == 0 && lane == 0) {
-      if (l_armed) mbar_wait(smem_u32(&ms->lfull), 0, limit, nullptr);
+      if (l_loads > 0) mbar_wait(smem_u32(&ms->lfull), (uint32_t)(l_loads - 1) & 1, limit, nullptr);
       for (int i = 0; i < kLStages; ++i)
         if (armed & (1u << i))
           mbar_wait(smem_u32(&ms->full[i]), (armed_par >> i) & 1, limit, nullptr);
@@ -786,7 +931,7 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
 }
 
 constexpr size_t gram_smem() {
-  return 1024 + (kGStages + 2) * (size_t)kJTileBytes + sizeof(GramSmem);
+  return 1024 + kGStages * (size_t)kJTileBytes + sizeof(GramSmem);
 }
 
 constexpr size_t lev_smem() {
@@ -819,12 +964,11 @@ cudaError_t launch_jacap(const JacapArgs& a) {
     if ((e = cudaFuncSetAttribute(jacap_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)))
       return e;
-    if (a.layers * a.splits_per_layer > 0)
-      jacap_gram_kernel<<<(unsigned)(a.layers * a.splits_per_layer), kGThreads, smem, a.stream>>>(gp);
+    if (a.n_gram > 0) jacap_gram_kernel<<<(unsigned)a.n_gram, kGThreads, smem, a.stream>>>(gp);
     if ((e = cudaGetLastError())) return e;
   }
   {
-    const size_t smem = 2 * (size_t)kJD * kFLd * sizeof(float);
+    const size_t smem = (size_t)kJD * kJD * sizeof(float);
     if ((e = cudaFuncSetAttribute(jacap_factor_kernel,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
       return e;
@@ -844,8 +988,8 @@ cudaError_t launch_jacap(const JacapArgs& a) {
     if ((e = cudaFuncSetAttribute(jacap_leverage_kernel,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
       return e;
-    if (a.layers * a.lev_per_layer > 0)
-      jacap_leverage_kernel<<<(unsigned)(a.layers * a.lev_per_layer), kLThreads, smem, a.stream>>>(lp);
+    if (a.n_gram > 0)
+      jacap_leverage_kernel<<<(unsigned)a.n_gram, kLThreads, smem, a.stream>>>(lp);
     if ((e = cudaGetLastError())) return e;
   }
   return cudaSuccess;

@@ -168,11 +168,17 @@ struct JSeq {
   int32_t index;           // sequence number in the call (q_win row block)
   int32_t n_chunks;        // statistics chunks (kJChunk prefix rows each)
   int32_t chunk_base;      // first statistics item of (sequence, head 0) within a layer
-  int32_t n_split;         // Gram splits per head
-  int32_t split_base;      // first Gram item of (sequence, head 0) within a layer
-  int32_t n_lev;           // leverage items per head (kJLevTiles tiles each)
-  int32_t lev_base;        // first leverage item of (sequence, head 0) within a layer
   int32_t inst_base;       // instance id of (sequence, head 0) within a layer
+  int32_t pad;
+};
+
+// One piece of Gram work: tiles [t_begin, t_end) (kJTile tokens each) of one
+// instance. The Gram CTAs split the instances' tiles, in instance order, into
+// equal contiguous ranges; a range cut at instance boundaries gives the
+// pieces, numbered in that order, and piece s writes partial matrix s.
+struct JSeg {
+  int32_t inst;            // layer * inst_per_layer + instance id within the layer
+  int32_t t_begin, t_end;
   int32_t pad;
 };
 
@@ -184,11 +190,15 @@ struct JacapArgs {
   int64_t T;
   int n_scored;
   const JSeq* seqs;        // device: the scored sequences
-  int chunks_per_layer, splits_per_layer, lev_per_layer, inst_per_layer;
+  int chunks_per_layer, inst_per_layer;
+  int n_gram;              // Gram CTAs
+  const JSeg* segs;        // device: the pieces
+  const int32_t* cta_seg;  // device, n_gram + 1: CTA c takes pieces cta_seg[c] .. cta_seg[c+1]-1
+  const int32_t* inst_seg; // device, instances + 1: instance i's pieces (its partials, in order)
   float tau, beta, eps;
   float2* zk;              // [layers][H][T]: (z in base-2 units, kappa) per prefix token
   float* part;             // [statistics items][2]: base-2 max and sum of 2^z
-  float* gram;             // [Gram items][D][D] partial sums of w v v^T
+  float* gram;             // [pieces][D][D] partial sums of w v v^T
   float* wts;              // [layers][H][T]: w per prefix token
   void* linv;              // [instances][2][D][D] bf16: L^{-1} split into hi + lo
   float* scores;           // [layers][H][T]: r per prefix token
@@ -198,7 +208,7 @@ struct JacapArgs {
 };
 
 constexpr int kJChunk = 512;         // prefix rows per statistics item
-constexpr int kJLevTiles = 8;        // 128-token tiles per leverage item
+constexpr int kJGramMinTiles = 8;    // fewest tiles per Gram CTA (below that, fewer CTAs)
 
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
 constexpr int64_t kMaxPrefix = 262144;  // longest prefix L - W the select kernel takes
