@@ -726,7 +726,7 @@ namespace {
 // statistics, Gram and leverage item numbering (per layer).
 struct JacapPlan {
   std::vector<JSeq> seqs;
-  int chunks = 0, insts = 0;
+  int insts = 0;
   // Gram work: pieces, the pieces of each CTA and of each instance
   std::vector<JSeg> segs;
   std::vector<int32_t> cta_seg, inst_seg;
@@ -743,10 +743,7 @@ JacapPlan plan_jacap(const Plan& p, int W, int C, int sm_count) {
     j.tok_off = sd.tok_off;
     j.len = sd.len;
     j.index = sd.index;
-    j.n_chunks = (P + kJChunk - 1) / kJChunk;
-    j.chunk_base = jp.chunks;
     j.inst_base = jp.insts;
-    jp.chunks += p.H * j.n_chunks;
     jp.insts += p.H;
     jp.seqs.push_back(j);
     tiles_of.push_back(n_tiles);
@@ -797,7 +794,7 @@ size_t jacap_table_bytes(const JacapPlan& jp) {
 size_t jacap_ws_bytes(const Plan& p, const JacapPlan& jp) {
   const size_t plane = (size_t)p.layers * p.H * p.T;
   return 8 * 256 + plane * (sizeof(float2) + sizeof(float)) +
-         (size_t)p.layers * jp.chunks * 2 * sizeof(float) + jacap_table_bytes(jp) +
+         jp.segs.size() * 2 * sizeof(float) + jacap_table_bytes(jp) +
          jp.segs.size() * 128 * 128 * sizeof(float) +
          (size_t)p.layers * jp.insts * 2 * 128 * 128 * 2;
 }
@@ -809,17 +806,17 @@ kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const vo
                        float* scores, char* ws, Carve& cv, cudaStream_t s,
                        cudaEvent_t* ev = nullptr) {
   const std::vector<JSeq>& seqs = jp.seqs;
-  const int chunks = jp.chunks, insts = jp.insts;
+  const int insts = jp.insts;
   const size_t plane = (size_t)p.layers * p.H * p.T;
   cudaError_t e = cudaMemsetAsync(scores, 0, plane * sizeof(float), s);
   if (e) return cuda_fail(e, "cudaMemsetAsync(scores)");
   if (seqs.empty()) return KVSEL_OK;
-  if ((int64_t)p.layers * std::max(chunks, insts) > 0x7fffffffLL)
+  if ((int64_t)p.layers * insts > 0x7fffffffLL)
     return KVSEL_ERR_UNSUPPORTED;
   const size_t o_tab = cv.take(jacap_table_bytes(jp));
   const size_t o_zk = cv.take(plane * sizeof(float2));
   const size_t o_w = cv.take(plane * sizeof(float));
-  const size_t o_part = cv.take((size_t)p.layers * chunks * 2 * sizeof(float));
+  const size_t o_part = cv.take(jp.segs.size() * 2 * sizeof(float));
   const size_t o_gram = cv.take(jp.segs.size() * 128 * 128 * sizeof(float));
   const size_t o_linv = cv.take((size_t)p.layers * insts * 2 * 128 * 128 * 2);
   // the tables, packed as jacap_table_bytes lays them out
@@ -856,7 +853,6 @@ kvsel_status run_jacap(const Plan& p, const JacapPlan& jp, DevState* d, const vo
   a.cta_seg = reinterpret_cast<const int32_t*>(ws + o_tab + o_cta);
   a.inst_seg = reinterpret_cast<const int32_t*>(ws + o_tab + o_inst);
   a.n_gram = (int)(jp.cta_seg.size() - 1);
-  a.chunks_per_layer = chunks;
   a.inst_per_layer = insts;
   a.tau = tau;
   a.beta = beta;

@@ -48,158 +48,7 @@ constexpr int kJTile = 128;                   // tokens per MMA tile
 constexpr int kJTileBytes = kJTile * kJD * 2; // one V tile, bf16: 32 KiB
 constexpr int kAtom = kJTile * 128;           // one 64-column swizzle atom of a tile: 16 KiB
 
-template <typename F>
-__device__ __forceinline__ int find_jseq(const JacapArgs& a, int rem, F base_of) {
-  return upper_find(a.n_scored, rem, base_of);
-}
-
-// ---------------------------------------------------------------------------
-// stats
-// ---------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(256) jacap_stats_kernel(const __grid_constant__ JacapArgs a) {
-  __shared__ float mu_s[kJD], lam_s[kJD];
-  __shared__ float wm[8], wl[8];
-  __shared__ __align__(16) __nv_bfloat16 qs[32][kJD];   // 32 window queries at a time
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int item = blockIdx.x;
-  const int layer = item / a.chunks_per_layer;
-  const int rem = item - layer * a.chunks_per_layer;
-  const JSeq& sq = a.seqs[find_jseq(a, rem, [&](int i) { return a.seqs[i].chunk_base; })];
-  const int local = rem - sq.chunk_base;
-  const int h = local / sq.n_chunks, c = local - h * sq.n_chunks;
-  const int P = sq.len - a.W;
-  const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  // K rows: each warp takes 16 consecutive rows a trip, each 8-lane group
-  // four of them (rows wb + 4u + grp), every load issued before any use; the
-  // first trip's loads go out before the window statistics
-  const int grp = lane >> 3, sub = lane & 7;
-  const int r_begin = c * kJChunk, r_end = min(P, r_begin + kJChunk);
-  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(a.k);
-  uint4 kr[4][2];
-  auto load_trip = [&](int wb) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = min(wb + 4 * u + grp, r_end - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(
-          kb + (((int64_t)layer * a.T + sq.tok_off + j) * a.H + h) * kJD + sub * 16);
-      kr[u][0] = __ldcs(src);
-      kr[u][1] = __ldcs(src + 1);
-    }
-  };
-  int wb = r_begin + warp * 16;
-  if (wb < r_end) load_trip(wb);
-  {
-    // the window statistics: rows staged 32 at a time with every thread
-    // loading (16 bytes each), the recursion run by one thread per dimension
-    const int64_t row0 = (int64_t)layer * a.S * a.W + (int64_t)sq.index * a.W;
-    float mu = 0.f, m2 = 0.f;
-    for (int r0 = 0; r0 < a.W; r0 += 32) {
-      const int nr = min(32, a.W - r0);
-      for (int e = tid; e < nr * (kJD / 8); e += blockDim.x) {
-        const int r = e / (kJD / 8), c = e - r * (kJD / 8);
-        *reinterpret_cast<uint4*>(&qs[r][c * 8]) = *reinterpret_cast<const uint4*>(
-            qb + ((row0 + r0 + r) * a.H + h) * kJD + c * 8);
-      }
-      __syncthreads();
-      if (tid < kJD) {
-        for (int r = 0; r < nr; ++r) {
-          const float q = __bfloat162float(qs[r][tid]);
-          if (r0 + r == 0) {
-            mu = q;
-            m2 = q * q;
-          } else {
-            mu = a.beta * mu + (1.f - a.beta) * q;
-            m2 = a.beta * m2 + (1.f - a.beta) * (q * q);
-          }
-        }
-      }
-      __syncthreads();
-    }
-    if (tid < kJD) {
-      mu_s[tid] = mu * (1.4426950408889634f / (a.tau * sqrtf((float)kJD)));
-      lam_s[tid] = fmaxf(m2 - mu * mu, a.eps);
-    }
-  }
-  __syncthreads();
-  float mu[16], lam[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    mu[e] = mu_s[sub * 16 + e];
-    lam[e] = lam_s[sub * 16 + e];
-  }
-  const int64_t plane = ((int64_t)layer * a.H + h) * a.T + sq.tok_off;
-  float m = -INFINITY, l = 0.f;
-  while (wb < r_end) {                                       // warp-uniform trips
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t w[8] = {kr[u][0].x, kr[u][0].y, kr[u][0].z, kr[u][0].w,
-                             kr[u][1].x, kr[u][1].y, kr[u][1].z, kr[u][1].w};
-      float z = 0.f, kap = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float kv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-        z = fmaf(mu[e], kv, z);
-        kap = fmaf(lam[e] * kv, kv, kap);
-      }
-#pragma unroll
-      for (int off = 1; off < 8; off <<= 1) {
-        z += __shfl_xor_sync(0xffffffffu, z, off);
-        kap += __shfl_xor_sync(0xffffffffu, kap, off);
-      }
-      const int row = wb + 4 * u + grp;
-      if (row < r_end) {
-        if (sub == 0) a.zk[plane + row] = make_float2(z, kap);
-        const float mx = fmaxf(m, z);
-        l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + ex2(z - mx);
-        m = mx;
-      }
-    }
-    wb += 128;
-    if (wb < r_end) load_trip(wb);
-  }
-#pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
-    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-    const float lo = __shfl_xor_sync(0xffffffffu, l, off);
-    const float mx = fmaxf(m, mo);
-    l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + (mo == -INFINITY ? 0.f : lo * ex2(mo - mx));
-    m = mx;
-  }
-  if (lane == 0) {
-    wm[warp] = m;
-    wl[warp] = l;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float mx = -INFINITY, sum = 0.f;
-    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, wm[w]);
-    for (int w = 0; w < 8; ++w)
-      if (wm[w] != -INFINITY) sum = fmaf(wl[w], ex2(wm[w] - mx), sum);
-    a.part[2 * (int64_t)item] = mx;
-    a.part[2 * (int64_t)item + 1] = sum;
-    if (!finite_f(mx) || !finite_f(sum)) record_status(a.status, KVSEL_ERR_NONFINITE);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// gram
-// ---------------------------------------------------------------------------
-
-constexpr int kGStages = 6;                    // V tile ring
-constexpr int kGThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 scale
-constexpr int kGWork = 256;                    // scaling threads
-
-struct GramSmem {
-  unsigned long long full[kGStages], empty[kGStages];   // V ring: loaded, free
-  unsigned long long scaled[kGStages];                  // V ring: scaled by sqrt(w)
-  unsigned long long done[2], tfree[2];                 // TMEM accumulators (one per piece)
-  unsigned long long drain;                    // abort path: the MMA issuer's last commit
-  uint32_t tmem_base;
-  int abort_flag;
-  float norm_m, norm_s;                        // the piece's instance: base-2 softmax max and sum
-  float sw[2][kJTile];                         // sqrt(w) of a tile's tokens (double buffer)
-};
+constexpr int kWork = 256;                     // compute threads of the stats and Gram kernels
 
 // The instance of a Gram piece: layer, sequence, head.
 struct JInst {
@@ -216,13 +65,8 @@ __device__ __forceinline__ JInst jinst(const JacapArgs& a, int inst) {
   return r;
 }
 
-struct GramParams {
-  CUtensorMap tmv;                             // V as (D, H, layers * T)
-  JacapArgs a;
-};
-
 __device__ __forceinline__ void work_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kGWork) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kWork) : "memory");
 }
 
 // Barrier of the scaling threads that also returns, in every one of them,
@@ -235,10 +79,260 @@ __device__ __forceinline__ bool work_bar_any(bool v) {
       "bar.red.or.pred po, 1, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)v), "n"(kGWork)
+      : "r"((uint32_t)v), "n"(kWork)
       : "memory");
   return r != 0;
 }
+
+// ---------------------------------------------------------------------------
+// stats
+// ---------------------------------------------------------------------------
+
+constexpr int kSStages = 6;                    // K tile ring
+constexpr int kSThreads = 32 + kWork;          // warp 0 TMA, warps 1..8 compute
+
+struct StatsSmem {
+  unsigned long long full[kSStages], empty[kSStages];
+  int abort_flag;
+  float mu[kJD], lam[kJD];                     // mu scaled to base-2 logits; diag Lambda
+  float wm[kWork / 32], wl[kWork / 32];
+  __align__(16) __nv_bfloat16 qs[32][kJD];     // 32 window queries at a time
+};
+
+struct StatsParams {
+  CUtensorMap tmk;                             // K as (D, H, layers * T)
+  JacapArgs a;
+};
+
+// Persistent over the pieces (the Gram kernel's CTA ranges): per piece the
+// window statistics of its instance (the W x d recursion, queries staged 32
+// rows at a time), then per K tile (TMA, 128-byte swizzle) z (base-2 units)
+// and kappa per token, eight lanes per token (lane s takes 16-byte chunk s of
+// both 64-dimension halves: a quarter-warp reads one 128-byte row, no bank
+// conflicts), and the piece's max and sum of 2^z. HBM-bound on K.
+__global__ void __launch_bounds__(kSThreads, 1)
+jacap_stats_kernel(const __grid_constant__ StatsParams S) {
+  const JacapArgs& a = S.a;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sk = smem;                                   // kSStages x 32 KiB
+  StatsSmem* ms = reinterpret_cast<StatsSmem*>(sk + kSStages * kJTileBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = a.wait_limit_ns;
+  volatile int* abort_flag = &ms->abort_flag;
+  const int s_begin = a.cta_seg[blockIdx.x], s_end = a.cta_seg[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSStages; ++i) {
+      mbar_init(smem_u32(&ms->full[i]), 1);
+      mbar_init(smem_u32(&ms->empty[i]), kWork / 32);
+    }
+    ms->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t armed = 0, armed_par = 0;
+
+  if (warp == 0) {
+    // ---- TMA producer: the K tiles of every piece, in order
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int sg = s_begin; ok && sg < s_end; ++sg) {
+        const JSeg pc = a.segs[sg];
+        const JInst in = jinst(a, pc.inst);
+        const int64_t row0 = (int64_t)in.layer * a.T + in.sq->tok_off;
+        for (int t = pc.t_begin; t < pc.t_end; ++t) {
+          if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
+            *abort_flag = 1;
+            record_status(a.status, KVSEL_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&ms->full[stage]);
+          mbar_expect_tx(bar, kJTileBytes);
+          const int row = (int)(row0 + (int64_t)t * kJTile);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem_u32(sk + stage * kJTileBytes + hf * kAtom), &S.tmk, bar, hf * 64, in.h,
+                        row, pol);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kSStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else {
+    // ---- compute warps (1..8)
+    const int tid = threadIdx.x - 32, cw = tid >> 5;
+    const int grp = lane >> 3, sub = lane & 7;
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int sg = s_begin; sg < s_end; ++sg) {
+      const JSeg pc = a.segs[sg];
+      const JInst in = jinst(a, pc.inst);
+      const int P = in.sq->len - a.W;
+      const int64_t plane = ((int64_t)in.layer * a.H + in.h) * a.T + in.sq->tok_off;
+      {
+        // the window statistics: mu <- beta mu + (1 - beta) q and m <- beta m +
+        // (1 - beta) q^2 over the W window queries from the first, one thread
+        // per dimension
+        const int64_t qrow0 = (int64_t)in.layer * a.S * a.W + (int64_t)in.sq->index * a.W;
+        float mu = 0.f, m2 = 0.f;
+        for (int r0 = 0; r0 < a.W; r0 += 32) {
+          const int nr = min(32, a.W - r0);
+          for (int e = tid; e < nr * (kJD / 8); e += kWork) {
+            const int r = e / (kJD / 8), c = e - r * (kJD / 8);
+            *reinterpret_cast<uint4*>(&ms->qs[r][c * 8]) = *reinterpret_cast<const uint4*>(
+                qb + ((qrow0 + r0 + r) * a.H + in.h) * kJD + c * 8);
+          }
+          work_bar();
+          if (tid < kJD) {
+            for (int r = 0; r < nr; ++r) {
+              const float q = __bfloat162float(ms->qs[r][tid]);
+              if (r0 + r == 0) {
+                mu = q;
+                m2 = q * q;
+              } else {
+                mu = a.beta * mu + (1.f - a.beta) * q;
+                m2 = a.beta * m2 + (1.f - a.beta) * (q * q);
+              }
+            }
+          }
+          work_bar();
+        }
+        if (tid < kJD) {
+          ms->mu[tid] = mu * (1.4426950408889634f / (a.tau * sqrtf((float)kJD)));
+          ms->lam[tid] = fmaxf(m2 - mu * mu, a.eps);
+        }
+        work_bar();
+      }
+      // lane sub: dimensions 8 sub .. 8 sub + 7 and 64 + 8 sub .. 64 + 8 sub + 7
+      float mu[16], lam[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int d = (e >> 3) * 64 + sub * 8 + (e & 7);
+        mu[e] = ms->mu[d];
+        lam[e] = ms->lam[d];
+      }
+      float m = -INFINITY, l = 0.f;
+      for (int t = pc.t_begin; t < pc.t_end; ++t) {
+        if (ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag));
+          if (ok) {
+            const unsigned char* kt = sk + stage * kJTileBytes;
+#pragma unroll
+            for (int step = 0; step < kJTile / 32; ++step) {
+              const int row = step * 32 + cw * 4 + grp;
+              const uint32_t off = (uint32_t)(row * 128 + ((sub ^ (row & 7)) << 4));
+              const uint4 k0 = *reinterpret_cast<const uint4*>(kt + off);
+              const uint4 k1 = *reinterpret_cast<const uint4*>(kt + kAtom + off);
+              const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+              float z = 0.f, kap = 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float kv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+                z = fmaf(mu[e], kv, z);
+                kap = fmaf(lam[e] * kv, kv, kap);
+              }
+#pragma unroll
+              for (int off2 = 1; off2 < 8; off2 <<= 1) {
+                z += __shfl_xor_sync(0xffffffffu, z, off2);
+                kap += __shfl_xor_sync(0xffffffffu, kap, off2);
+              }
+              const int tok = t * kJTile + row;
+              if (tok < P) {
+                if (sub == 0) a.zk[plane + tok] = make_float2(z, kap);
+                const float mx = fmaxf(m, z);
+                l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + ex2(z - mx);
+                m = mx;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ms->empty[stage]));
+          }
+        }
+        if (++stage == kSStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // the piece's max and sum: lane groups, then warps; a wait given up
+      // anywhere ends every compute warp here
+      if (work_bar_any(!ok)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int off2 = 8; off2 <= 16; off2 <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off2);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, off2);
+        const float mx = fmaxf(m, mo);
+        l = (m == -INFINITY ? 0.f : l * ex2(m - mx)) + (mo == -INFINITY ? 0.f : lo * ex2(mo - mx));
+        m = mx;
+      }
+      if (lane == 0) {
+        ms->wm[cw] = m;
+        ms->wl[cw] = l;
+      }
+      work_bar();
+      if (tid == 0) {
+        float mx = -INFINITY, sum = 0.f;
+        for (int w = 0; w < kWork / 32; ++w) mx = fmaxf(mx, ms->wm[w]);
+        for (int w = 0; w < kWork / 32; ++w)
+          if (ms->wm[w] != -INFINITY) sum = fmaf(ms->wl[w], ex2(ms->wm[w] - mx), sum);
+        a.part[2 * (int64_t)sg] = mx;
+        a.part[2 * (int64_t)sg + 1] = sum;
+        if (!finite_f(mx) || !finite_f(sum)) record_status(a.status, KVSEL_ERR_NONFINITE);
+      }
+      // wm, wl, mu, lam and qs are rewritten by the next piece only after this
+      work_bar();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_status(a.status, KVSEL_ERR_TIMEOUT);
+    }
+  }
+
+  __syncthreads();
+  if (ms->abort_flag && warp == 0 && lane == 0) {
+    for (int i = 0; i < kSStages; ++i)
+      if (armed & (1u << i))
+        mbar_wait(smem_u32(&ms->full[i]), (armed_par >> i) & 1, limit, nullptr);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gram
+// ---------------------------------------------------------------------------
+
+constexpr int kGStages = 6;                    // V tile ring
+constexpr int kGThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 scale
+
+struct GramSmem {
+  unsigned long long full[kGStages], empty[kGStages];   // V ring: loaded, free
+  unsigned long long scaled[kGStages];                  // V ring: scaled by sqrt(w)
+  unsigned long long done[2], tfree[2];                 // TMEM accumulators (one per piece)
+  unsigned long long drain;                    // abort path: the MMA issuer's last commit
+  uint32_t tmem_base;
+  int abort_flag;
+  float norm_m, norm_s;                        // the piece's instance: base-2 softmax max and sum
+  float sw[2][kJTile];                         // sqrt(w) of a tile's tokens (double buffer)
+};
+
+struct GramParams {
+  CUtensorMap tmv;                             // V as (D, H, layers * T)
+  JacapArgs a;
+};
 
 // Shared-memory descriptor of a V tile read MN-major (dimensions as M or N,
 // tokens as K), 128-byte swizzle as TMA wrote it: 64 dimensions per 128-byte
@@ -391,14 +485,14 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
       const int P = sq.len - a.W;
       const int64_t plane = ((int64_t)in.layer * a.H + in.h) * a.T + sq.tok_off;
       if (wq == 0) {
-        // merge the instance's statistics partials in a fixed order
-        const float* pr = a.part + 2 * ((int64_t)in.layer * a.chunks_per_layer + sq.chunk_base +
-                                        (int64_t)in.h * sq.n_chunks);
+        // merge the instance's statistics partials (one per piece) in order
+        const int p0 = a.inst_seg[pc.inst], np = a.inst_seg[pc.inst + 1] - p0;
+        const float* pr = a.part + 2 * (int64_t)p0;
         float mx = -INFINITY;
-        for (int c = lid; c < sq.n_chunks; c += 32) mx = fmaxf(mx, pr[2 * c]);
+        for (int c = lid; c < np; c += 32) mx = fmaxf(mx, pr[2 * c]);
         for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         float sum = 0.f;
-        for (int c = lid; c < sq.n_chunks; c += 32) sum = fmaf(pr[2 * c + 1], ex2(pr[2 * c] - mx), sum);
+        for (int c = lid; c < np; c += 32) sum = fmaf(pr[2 * c + 1], ex2(pr[2 * c] - mx), sum);
         for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         if (lid == 0) {
           ms->norm_m = mx;
@@ -440,8 +534,8 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
           unsigned char* vt = sv + stage * kJTileBytes;
           const float* sw = ms->sw[i & 1];
 #pragma unroll
-          for (int j = 0; j < kJTileBytes / 16 / kGWork; ++j) {
-            const int e = tid + kGWork * j;
+          for (int j = 0; j < kJTileBytes / 16 / kWork; ++j) {
+            const int e = tid + kWork * j;
             const float f = sw[(e >> 3) & (kJTile - 1)];
             uint4* p = reinterpret_cast<uint4*>(vt + e * 16);
             uint4 x = *p;
@@ -930,6 +1024,10 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr size_t stats_smem() {
+  return 1024 + kSStages * (size_t)kJTileBytes + sizeof(StatsSmem);
+}
+
 constexpr size_t gram_smem() {
   return 1024 + kGStages * (size_t)kJTileBytes + sizeof(GramSmem);
 }
@@ -952,9 +1050,18 @@ cudaError_t launch_jacap(const JacapArgs& a) {
   const int64_t rows = (int64_t)a.layers * a.T;
   if (rows >= 0x7fffffffLL) return cudaErrorInvalidValue;
   cudaError_t e;
-  if (a.layers * a.chunks_per_layer > 0)
-    jacap_stats_kernel<<<(unsigned)(a.layers * a.chunks_per_layer), 256, 0, a.stream>>>(a);
-  if ((e = cudaGetLastError())) return e;
+  {
+    StatsParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if (!make_rows_map(&sp.tmk, a.k, kJD, a.H, rows, 1, kJTile)) return cudaErrorInvalidValue;
+    sp.a = a;
+    const size_t smem = stats_smem();
+    if ((e = cudaFuncSetAttribute(jacap_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)))
+      return e;
+    if (a.n_gram > 0) jacap_stats_kernel<<<(unsigned)a.n_gram, kSThreads, smem, a.stream>>>(sp);
+    if ((e = cudaGetLastError())) return e;
+  }
   {
     GramParams gp;
     std::memset(&gp, 0, sizeof(gp));

@@ -166,8 +166,6 @@ struct JSeq {
   int64_t tok_off;         // first token of the sequence within a layer
   int32_t len;             // L
   int32_t index;           // sequence number in the call (q_win row block)
-  int32_t n_chunks;        // statistics chunks (kJChunk prefix rows each)
-  int32_t chunk_base;      // first statistics item of (sequence, head 0) within a layer
   int32_t inst_base;       // instance id of (sequence, head 0) within a layer
   int32_t pad;
 };
@@ -190,14 +188,14 @@ struct JacapArgs {
   int64_t T;
   int n_scored;
   const JSeq* seqs;        // device: the scored sequences
-  int chunks_per_layer, inst_per_layer;
+  int inst_per_layer;
   int n_gram;              // Gram CTAs
   const JSeg* segs;        // device: the pieces
   const int32_t* cta_seg;  // device, n_gram + 1: CTA c takes pieces cta_seg[c] .. cta_seg[c+1]-1
   const int32_t* inst_seg; // device, instances + 1: instance i's pieces (its partials, in order)
   float tau, beta, eps;
   float2* zk;              // [layers][H][T]: (z in base-2 units, kappa) per prefix token
-  float* part;             // [statistics items][2]: base-2 max and sum of 2^z
+  float* part;             // [pieces][2]: base-2 max and sum of 2^z over the piece's tokens
   float* gram;             // [pieces][D][D] partial sums of w v v^T
   float* wts;              // [layers][H][T]: w per prefix token
   void* linv;              // [instances][2][D][D] bf16: L^{-1} split into hi + lo
@@ -207,7 +205,6 @@ struct JacapArgs {
   cudaStream_t stream;
 };
 
-constexpr int kJChunk = 512;         // prefix rows per statistics item
 constexpr int kJGramMinTiles = 8;    // fewest tiles per Gram CTA (below that, fewer CTAs)
 
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
