@@ -48,7 +48,9 @@ constexpr int kJTile = 128;                   // tokens per MMA tile
 constexpr int kJTileBytes = kJTile * kJD * 2; // one V tile, bf16: 32 KiB
 constexpr int kAtom = kJTile * 128;           // one 64-column swizzle atom of a tile: 16 KiB
 
-constexpr int kWork = 256;                     // compute threads of the stats and Gram kernels
+constexpr int kWork = 512;                     // compute threads of the stats and Gram kernels
+static_assert(kWork % 128 == 0 && kWork <= 1024 - 64, "whole lane quarters, one CTA");
+static_assert(kJTile % (kWork / 8) == 0 && (kJTileBytes / 16) % kWork == 0, "whole steps per tile");
 
 // The instance of a Gram piece: layer, sequence, head.
 struct JInst {
@@ -89,7 +91,7 @@ __device__ __forceinline__ bool work_bar_any(bool v) {
 // ---------------------------------------------------------------------------
 
 constexpr int kSStages = 6;                    // K tile ring
-constexpr int kSThreads = 32 + kWork;          // warp 0 TMA, warps 1..8 compute
+constexpr int kSThreads = 32 + kWork;          // warp 0 TMA, warps 1.. compute
 
 struct StatsSmem {
   unsigned long long full[kSStages], empty[kSStages];
@@ -170,7 +172,7 @@ jacap_stats_kernel(const __grid_constant__ StatsParams S) {
       }
     }
   } else {
-    // ---- compute warps (1..8)
+    // ---- compute warps (1 ..)
     const int tid = threadIdx.x - 32, cw = tid >> 5;
     const int grp = lane >> 3, sub = lane & 7;
     const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
@@ -231,8 +233,8 @@ jacap_stats_kernel(const __grid_constant__ StatsParams S) {
           if (ok) {
             const unsigned char* kt = sk + stage * kJTileBytes;
 #pragma unroll
-            for (int step = 0; step < kJTile / 32; ++step) {
-              const int row = step * 32 + cw * 4 + grp;
+            for (int step = 0; step < kJTile / (kWork / 8); ++step) {
+              const int row = step * (kWork / 8) + cw * 4 + grp;
               const uint32_t off = (uint32_t)(row * 128 + ((sub ^ (row & 7)) << 4));
               const uint4 k0 = *reinterpret_cast<const uint4*>(kt + off);
               const uint4 k1 = *reinterpret_cast<const uint4*>(kt + kAtom + off);
@@ -316,7 +318,7 @@ jacap_stats_kernel(const __grid_constant__ StatsParams S) {
 // ---------------------------------------------------------------------------
 
 constexpr int kGStages = 6;                    // V tile ring
-constexpr int kGThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 scale
+constexpr int kGThreads = 64 + kWork;          // warp 0 TMA, warp 1 MMA, warps 2.. scale
 
 struct GramSmem {
   unsigned long long full[kGStages], empty[kGStages];   // V ring: loaded, free
@@ -468,7 +470,7 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
       }
     }
   } else {
-    // ---- scaling warps (2..9): per piece the instance's softmax normaliser,
+    // ---- scaling warps (2 ..): per piece the instance's softmax normaliser,
     // then per tile w and the tile scaled by sqrt(w); at the end of the piece
     // its partial Gram out of TMEM
     const int tid = threadIdx.x - 64;
@@ -519,16 +521,23 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
           ms->sw[buf][tid] = sqrtf(w);
         }
       };
-      float2 z1 = fetch(pc.t_begin + 1), z2 = fetch(pc.t_begin + 2);
+      // zo, ze: (z, kappa) of the piece's odd and even tiles (tile - t_begin),
+      // each loaded two tiles before its use; the parity branch keeps both in
+      // place (no register copy waits on a load in flight)
+      float2 zo = fetch(pc.t_begin + 1), ze = fetch(pc.t_begin + 2);
       weigh(pc.t_begin, i & 1, fetch(pc.t_begin));
       work_bar();
       // scaling in place: thread tid takes the 16-byte chunks tid + 256 j of
       // the tile (row (chunk / 8) % 128 of atom chunk / 1024; the swizzle only
       // permutes chunks within a row)
       for (int t = pc.t_begin; t < pc.t_end; ++t, ++i) {
-        if (t + 1 < pc.t_end) weigh(t + 1, (i + 1) & 1, z1);
-        z1 = z2;
-        z2 = fetch(t + 3);
+        if (((t - pc.t_begin) & 1) == 0) {
+          if (t + 1 < pc.t_end) weigh(t + 1, (i + 1) & 1, zo);
+          zo = fetch(t + 3);
+        } else {
+          if (t + 1 < pc.t_end) weigh(t + 1, (i + 1) & 1, ze);
+          ze = fetch(t + 3);
+        }
         const bool mine = mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag);
         if (mine) {
           unsigned char* vt = sv + stage * kJTileBytes;
@@ -563,7 +572,8 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
       }
       if (!ok) break;
       // the piece's partial: TMEM lanes are dimensions d1, columns d2; warp
-      // w reads lane quarter w % 4 and column half (w - 2) / 4
+      // w reads lane quarter w % 4 and the 128 / (kWork / 128) columns of
+      // group (w - 2) / 4
       const int ab = k & 1;
       const bool mine = mbar_wait(smem_u32(&ms->done[ab]), (uint32_t)(k >> 1) & 1, limit, abort_flag);
       if (work_bar_any(!mine)) {
@@ -571,13 +581,14 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
         break;
       }
       tc_fence_after();
-      const int quarter = warp & 3, half = (warp - 2) >> 2;
+      constexpr int kCols = kJD / (kWork / 128);
+      const int quarter = warp & 3, cg = (warp - 2) >> 2;
       const int d1 = quarter * 32 + lane;
-      float* out = a.gram + ((int64_t)sg * kJD + d1) * kJD + half * 64;
+      float* out = a.gram + ((int64_t)sg * kJD + d1) * kJD + cg * kCols;
 #pragma unroll
-      for (int cblk = 0; cblk < 64; cblk += 32) {
+      for (int cblk = 0; cblk < kCols; cblk += 32) {
         float v[32];
-        tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kJD + half * 64 + cblk,
+        tmem_load_cols<32>(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kJD + cg * kCols + cblk,
                            v);
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
@@ -621,9 +632,9 @@ jacap_gram_kernel(const __grid_constant__ GramParams G) {
 
 constexpr int kFB = kJD / 8;                   // 8 x 8 blocks per side
 
-// One CTA per instance, 256 threads; thread (bi, bk) = (tid / 16, tid % 16)
-// holds block (bi, bk) of the matrix in registers (the lower blocks bk <= bi
-// take part). Both phases are right-looking, one column (row) per step and
+// One CTA per instance, 160 threads: thread tid < 136 holds the lower block
+// (bi, bk), bk <= bi, numbered row by row (tid = bi (bi + 1) / 2 + bk), in
+// registers; three CTAs fit an SM (registers and shared memory). Both phases are right-looking, one column (row) per step and
 // one barrier per step:
 //   Cholesky  step j: the owners of column j (bk = j / 8) store its current
 //             values to shared memory; every thread reads the pivot d = A[j][j]
@@ -636,14 +647,21 @@ constexpr int kFB = kJD / 8;                   // 8 x 8 blocks per side
 //             B[i][:] -= L[i][j] X[j][:].
 // Entries above the diagonal of a diagonal block collect values that are
 // never read; the output writes zeros there.
-__global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
+constexpr int kFThreads = 160;
+constexpr int kFBlocks = kFB * (kFB + 1) / 2;   // 136 lower blocks
+
+__global__ void __launch_bounds__(kFThreads) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
   extern __shared__ float4 fs4[];
   float* Lc = reinterpret_cast<float*>(fs4);    // [kJD][kJD]: column j of the updated matrix at step j
   __shared__ float dinv[kJD];                   // 1 / L[j][j]
   __shared__ __align__(16) float xrow[2][kJD];  // X[j][:] of the current inverse step
   __shared__ int bad;
-  const int tid = threadIdx.x, bi = tid >> 4, bk = tid & (kFB - 1);
-  const bool act = bk <= bi;
+  const int tid = threadIdx.x;
+  const bool act = tid < kFBlocks;
+  int bi = 0;
+  while (bi < kFB - 1 && (bi + 1) * (bi + 2) / 2 <= tid) ++bi;
+  int bk = tid - bi * (bi + 1) / 2;
+  if (!act) bi = -1, bk = kFB;                  // idle: matches no owner or update test
   const int inst = blockIdx.x;
   const int s_lo = a.inst_seg[inst], n_part = a.inst_seg[inst + 1] - s_lo;
   if (tid == 0) bad = 0;
@@ -752,9 +770,19 @@ __global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant
     }
   }
 
-  // ---- output: rows bi*8 .. of L^{-1}, columns bk*8 .., as bf16 hi and lo
+  // ---- output: rows bi*8 .. of L^{-1}, columns bk*8 .., as bf16 hi and lo;
+  // the blocks above the diagonal are zero
   __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(a.linv) + (int64_t)inst * 2 * kJD * kJD;
   __nv_bfloat16* lo = hi + kJD * kJD;
+  for (int e = tid; e < kFB * kFB * 8; e += kFThreads) {
+    const int blk = e >> 3, r = e & 7, ui = blk / kFB, uk = blk - ui * kFB;
+    if (uk > ui) {
+      const int64_t off = (int64_t)(ui * 8 + r) * kJD + uk * 8;
+      *reinterpret_cast<uint4*>(hi + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(lo + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (act) {
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     uint32_t ph[4], pl[4];
@@ -770,6 +798,7 @@ __global__ void __launch_bounds__(256) jacap_factor_kernel(const __grid_constant
     const int64_t off = (int64_t)(bi * 8 + r) * kJD + bk * 8;
     *reinterpret_cast<uint4*>(hi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+  }
   }
   __syncthreads();
   if (tid == 0 && bad) record_status(a.status, KVSEL_ERR_NONFINITE);
@@ -1080,7 +1109,7 @@ cudaError_t launch_jacap(const JacapArgs& a) {
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
       return e;
     if (a.layers * a.inst_per_layer > 0)
-      jacap_factor_kernel<<<(unsigned)(a.layers * a.inst_per_layer), 256, smem, a.stream>>>(a);
+      jacap_factor_kernel<<<(unsigned)(a.layers * a.inst_per_layer), kFThreads, smem, a.stream>>>(a);
     if ((e = cudaGetLastError())) return e;
   }
   {
