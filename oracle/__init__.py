@@ -33,3 +33,4 @@ from .jacap_oracle import (  # noqa: F401,E402
     weights,
     window_statistics,
 )
+from .reverse_oracle import reverse_attention, reverse_packed  # noqa: F401,E402
