@@ -278,6 +278,37 @@ kvsel_status kvsel_decode_attention(const kvsel_shape* shape, const void* q, con
                                     const void* V, int32_t g, const void* K_new,
                                     const void* V_new, float* out, float* lse, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Reverse-mask attention of the counter-causal scorer (page "来自未来的信号：
+ * 用反因果惊奇度做 KV Cache 淘汰" (signals from the future: KV-cache eviction by
+ * counter-causal surprise), section 3.2, steps 1, 3 and 5; section 4,
+ * Algorithm 3). The part that needs no model weights: every cached row i of
+ * a sequence attends, with the scale 1/sqrt(D), to the cached rows j of the
+ * same sequence whose original position is larger than its own (a strictly
+ * upper-triangular mask in position order), reusing the cached K and V with
+ * queries recomputed at the original positions.
+ * ------------------------------------------------------------------------- */
+
+/* out_i = sum_{j: pos_j > pos_i} softmax_j(q_i . k_j / sqrt(D)) v_j and lse_i
+ * = ln sum_j exp(q_i . k_j / sqrt(D)) over the same j; a row with no such j
+ * (the last position) gets out = 0 and lse = -inf (the page gives it the
+ * largest surprise). `shape`: seq_offsets are the cache rows of each sequence,
+ * num_heads the query heads H, num_kv_heads (0 = H) the cache heads; query head
+ * h reads cache head h / (H / H_kv). Layouts (bf16, D = 128, rows 16-byte
+ * aligned): Q [num_layers][T][H][D]; K, V [num_layers][T][H_kv][D];
+ * positions [T] int32, the sequence-relative original position of each row
+ * (NULL: the row order; a refresh that reorders the memory passes them; equal
+ * positions do not attend to each other). Outputs (fp32, caller-owned device
+ * memory): out [num_layers][T][H][D] (16-byte aligned); lse
+ * [num_layers][H][T] natural log, or NULL. Rules: INVALID_ARG for NULL or
+ * misaligned pointers; UNSUPPORTED for a dtype other than bf16, D != 128,
+ * misaligned Q/K/V, or num_layers * T >= 2^31. Device status: NONFINITE if a
+ * row's max or sum is not finite; TIMEOUT if a bounded wait ran out.
+ * Asynchronous on `stream`. */
+kvsel_status kvsel_reverse_attention(const kvsel_shape* shape, const void* Q, const void* K,
+                                     const void* V, const int32_t* positions, float* out,
+                                     float* lse, void* stream);
+
 /* Per instance (n of them, e.g. layers * seqs * heads): the retained mass
  * mass[i] = exp(lse_keep[i] - lse_full[i]) (the full-cache probability of the
  * rows that the compacted cache kept, when lse_keep comes from the compacted

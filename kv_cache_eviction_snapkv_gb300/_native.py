@@ -45,6 +45,7 @@ SIGNATURES = {
     "kvsel_decode_attention": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                                        c_vp]),
     "kvsel_decode_quality": (c_i32, [c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "kvsel_reverse_attention": (c_i32, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "kvsel_cache_lengths": (c_i32, [_P, c_i32, c_i32, ctypes.POINTER(c_i64),
                                     ctypes.POINTER(c_i64)]),
     "kvsel_device_status": (c_i32, [c_vp]),

@@ -370,6 +370,32 @@ def kvsel_decode_attention(q, K, V, cache_offsets, K_new=None, V_new=None, g: in
     return out, lse
 
 
+def kvsel_reverse_attention(Q, K, V, seq_offsets, positions=None, out=None, lse=None,
+                            want_lse: bool = True, stream=None):
+    """(out [layers, T, H, D] fp32, lse [layers, H, T] fp32 or None): every row
+    i of a sequence attends to the rows of its sequence at later positions
+    only (positions [T] int32 sequence-relative, default the row order); a row
+    with no later row gets out = 0, lse = -inf. Q [layers, T, H, D]; K, V
+    [layers, T, H_kv, D]; bf16, D = 128."""
+    Q4, K4, V4 = _as4(Q), _as4(K), _as4(V)
+    L, T, H, D = Q4.shape
+    _need(K4, "K"), _need(V4, "V", K4.dtype), _need(Q4, "Q", K4.dtype)
+    sh = Shape(L, H, D, _DTYPES[K4.dtype], seq_offsets, num_kv_heads=K4.shape[2])
+    if positions is not None:
+        _need(positions, "positions", torch.int32)
+    if out is None:
+        out = torch.empty((L, T, H, D), dtype=torch.float32, device=K.device)
+    if lse is None and want_lse:
+        lse = torch.empty((L, H, T), dtype=torch.float32, device=K.device)
+    _need(out, "out", torch.float32)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    _check(_native.lib().kvsel_reverse_attention(sh.ref, _ptr(Q4), _ptr(K4), _ptr(V4),
+                                                 _ptr(positions), _ptr(out), _ptr(lse),
+                                                 _stream(stream)), "kvsel_reverse_attention")
+    return out, lse
+
+
 def kvsel_decode_quality(lse_keep, lse_full, out_keep, out_full, mass=None, err=None,
                          stream=None):
     """(mass, err), each shaped like lse: exp(lse_keep - lse_full) and

@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvsel.so")
 SOURCES = ["api.cu", "score_tc.cu", "score_generic.cu", "select.cu", "compact.cu",
-           "decode.cu", "jacap.cu"]
+           "decode.cu", "jacap.cu", "reverse.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1123,6 +1123,71 @@ kvsel_status kvsel_decode_attention(const kvsel_shape* shape, const void* q, con
   return cuda_fail(e, "decode attention launch");
 }
 
+kvsel_status kvsel_reverse_attention(const kvsel_shape* shape, const void* Q, const void* K,
+                                     const void* V, const int32_t* positions, float* out,
+                                     float* lse, void* stream) {
+  using namespace kvsel;
+  Plan p;
+  kvsel_status st;
+  if ((st = plan_shape(shape, 0, &p))) return st;
+  if (p.T == 0) return KVSEL_OK;
+  if (!Q || !K || !V || !out) return KVSEL_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 15) return KVSEL_ERR_INVALID_ARG;
+  if (!reverse_eligible(p.dtype, p.D, Q, K, V)) return KVSEL_ERR_UNSUPPORTED;
+  std::vector<RevSeq> seqs;
+  int64_t items = 0;
+  for (const SeqDesc& sd : p.all) {
+    if (sd.len == 0) continue;
+    RevSeq r{};
+    r.tok_off = sd.tok_off;
+    r.len = sd.len;
+    r.n_qt = (sd.len + 127) / 128;
+    r.item_base = (int32_t)items;
+    items += (int64_t)p.H * r.n_qt;
+    if (items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
+    seqs.push_back(r);
+  }
+  if ((int64_t)p.layers * items > 0x7fffffffLL || (int64_t)p.layers * p.T >= 0x7fffffffLL)
+    return KVSEL_ERR_UNSUPPORTED;
+  DevState* d;
+  if ((st = device_state(&d))) return st;
+  char* ws;
+  if ((st = workspace(d, seqs.size() * sizeof(RevSeq) + 256, &ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(ws, seqs.data(), seqs.size() * sizeof(RevSeq),
+                                  cudaMemcpyHostToDevice, s);
+  if (e) return cuda_fail(e, "cudaMemcpyAsync(reverse sequence table)");
+  RevArgs a{};
+  a.q = Q;
+  a.k = K;
+  a.v = V;
+  a.pos = positions;
+  a.out = out;
+  a.lse = lse;
+  a.layers = p.layers;
+  a.H = p.H;
+  a.Hkv = p.Hkv;
+  a.S = (int)seqs.size();
+  a.T = p.T;
+  a.seqs = reinterpret_cast<const RevSeq*>(ws);
+  a.items_per_layer = (int)items;
+  a.status = d->status;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_limit_ns = g_wait_limit_ns;
+  }
+  a.stream = s;
+  cudaEvent_t* ev = profile_slot();
+  if (ev) cudaEventRecord(ev[0], s);
+  e = launch_reverse(a);
+  if (ev) {
+    cudaEventRecord(ev[1], s);
+    cudaEventRecord(ev[2], s);
+    cudaEventRecord(ev[3], s);
+  }
+  return cuda_fail(e, "reverse attention launch");
+}
+
 kvsel_status kvsel_decode_quality(int64_t n, int32_t D, const float* lse_keep,
                                   const float* lse_full, const float* out_keep,
                                   const float* out_full, float* mass, float* err, void* stream) {

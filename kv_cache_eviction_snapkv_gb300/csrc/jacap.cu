@@ -336,19 +336,6 @@ struct GramParams {
   JacapArgs a;
 };
 
-// Shared-memory descriptor of a V tile read MN-major (dimensions as M or N,
-// tokens as K), 128-byte swizzle as TMA wrote it: 64 dimensions per 128-byte
-// row, the next 64 in the other atom (leading byte offset 16 KiB), the next 8
-// tokens 1 KiB on (stride byte offset).
-__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(kAtom >> 4) << 16;   // LBO
-  d |= (uint64_t)(1024 >> 4) << 32;    // SBO
-  d |= (uint64_t)1 << 46;              // descriptor version
-  d |= (uint64_t)2 << 61;              // 128-byte swizzle
-  return d;
-}
 
 __global__ void __launch_bounds__(kGThreads, 1)
 jacap_gram_kernel(const __grid_constant__ GramParams G) {
@@ -1040,18 +1027,6 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
 // Host
 // ---------------------------------------------------------------------------
 
-bool make_rows_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                   uint32_t box1, uint32_t box2) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  cuuint32_t box[3] = {64, box1, box2};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 constexpr size_t stats_smem() {
   return 1024 + kSStages * (size_t)kJTileBytes + sizeof(StatsSmem);

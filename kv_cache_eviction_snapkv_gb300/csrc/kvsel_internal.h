@@ -220,6 +220,36 @@ cudaError_t launch_compact(const CompactArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_jacap(const JacapArgs& a);
 bool jacap_eligible(int dtype, int D, const void* q, const void* k, const void* v);
+
+// Reverse-mask attention (counter-causal scorer): every cached row attends to
+// the rows of its sequence at later original positions only. One work item =
+// 128 query rows of one (layer, sequence, query head).
+struct RevSeq {
+  int64_t tok_off;         // first row of the sequence within a layer
+  int32_t len;             // rows n
+  int32_t n_qt;            // query tiles ceil(n / 128)
+  int32_t item_base;       // first item of the sequence within a layer (items qt * H + h)
+  int32_t pad;
+};
+
+struct RevArgs {
+  const void* q;           // [layers][T][H][D] bf16
+  const void* k;           // [layers][T][H_kv][D] bf16
+  const void* v;
+  const int32_t* pos;      // [T] sequence-relative original positions, or null (= row order)
+  float* out;              // [layers][T][H][D]
+  float* lse;              // [layers][H][T] natural log, or null
+  int layers, H, Hkv, S;
+  int64_t T;
+  const RevSeq* seqs;      // device
+  int items_per_layer;
+  int* status;
+  unsigned long long wait_limit_ns;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_reverse(const RevArgs& a);
+bool reverse_eligible(int dtype, int D, const void* q, const void* k, const void* v);
 cudaError_t launch_decode_quality(const QualityArgs& a);
 int decode_chunk_rows();
 bool decode_supported(int dtype, int D);

@@ -1,0 +1,396 @@
+// Reverse-mask attention of the counter-causal scorer: every cached row of a
+// sequence attends only to the rows at later original positions.
+//
+// Method: page "来自未来的信号：用反因果惊奇度做 KV Cache 淘汰" (signals from the
+// future: KV-cache eviction by counter-causal surprise), section 3.2, steps 1
+// (a strictly upper-triangular mask over the original order and position
+// ids), 3 (the cached K and V reused, queries at the original positions) and
+// 5 (the last position has no future context: out = 0, lse = -inf); section
+// 4, Algorithm 3 (a refresh reorders the memory by surprise, so the mask
+// follows the rows' positions when they are given).
+//
+// One CTA per 128 query rows of one (layer, sequence, query head); bf16,
+// D = 128; 192 threads: warp 0 TMA, warp 1 MMA, warps 2..5 softmax (one query
+// row per thread, TMEM lane quarter warp % 4).
+//   pass 1  S = Q K^T per 128-key tile (tcgen05, M = 128 queries, N = 128
+//           keys, K = D; two TMEM S buffers so the next tile's MMAs overlap
+//           this tile's softmax), then per row the max m and the sum l of
+//           2^x, x = S log2(e) / sqrt(D), over the allowed keys;
+//   pass 2  S again; P = 2^(x - m) / l in fp32 for the allowed keys (0
+//           elsewhere), split into bf16 hi = bf16(P) and lo = bf16(P - hi),
+//           written K-major (keys as K) to shared memory; O += P_hi V + P_lo V
+//           (tcgen05, V read MN-major as TMA wrote it), O in TMEM; at the end
+//           O (already normalised) and lse = (m + log2 l) ln 2 are written.
+// The producer loads in the order the MMA issuer consumes: pass 1 K tiles,
+// then K(0), and per tile t: K(t + 1), V(t) (S(t + 1) is issued before
+// P(t) V(t)). With positions in row order, key tiles before the query tile
+// hold no allowed key and are skipped; with explicit positions every key tile
+// of the sequence is visited.
+// Every wait is bounded (KVSEL_ERR_TIMEOUT, then the roles drain and return).
+#include <cmath>
+#include <cstring>
+
+#include "kvsel_device.cuh"
+#include "tc_common.cuh"
+
+namespace kvsel {
+namespace {
+
+constexpr int kRD = 128;                          // head dimension
+constexpr int kRTile = 128;                       // query rows and keys per tile
+constexpr int kRTileBytes = kRTile * kRD * 2;     // one bf16 tile: 32 KiB
+constexpr int kRAtom = kRTile * 128;              // one 64-column swizzle atom: 16 KiB
+constexpr int kRStages = 3;                       // K / V ring
+constexpr int kRThreads = 192;
+
+struct RevSmem {
+  unsigned long long qfull;
+  unsigned long long full[kRStages], empty[kRStages];
+  unsigned long long s_full[2], s_free[2];        // TMEM S buffers
+  unsigned long long p_full, p_free;              // P (hi, lo) in shared memory
+  unsigned long long o_done;
+  unsigned long long drain;                       // abort path: the MMA issuer's last commit
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct RevParams {
+  CUtensorMap tmq;                                // Q as (D, H, layers * T)
+  CUtensorMap tmk;                                // K as (D, H_kv, layers * T)
+  CUtensorMap tmv;                                // V likewise
+  RevArgs a;
+};
+
+__global__ void __launch_bounds__(kRThreads, 1)
+reverse_kernel(const __grid_constant__ RevParams R) {
+  const RevArgs& a = R.a;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* s_q = smem;                                  // Q tile
+  unsigned char* s_r = s_q + kRTileBytes;                     // kRStages x 32 KiB
+  unsigned char* s_p = s_r + kRStages * kRTileBytes;          // P hi, P lo
+  RevSmem* ms = reinterpret_cast<RevSmem*>(s_p + 2 * kRTileBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = a.wait_limit_ns;
+  volatile int* abort_flag = &ms->abort_flag;
+
+  // the work item: (layer, sequence, query tile qt, head h), qt-major
+  const int layer = blockIdx.x / a.items_per_layer;
+  const int rem = blockIdx.x - layer * a.items_per_layer;
+  const RevSeq& sq = a.seqs[upper_find(a.S, rem, [&](int i) { return a.seqs[i].item_base; })];
+  const int local = rem - sq.item_base;
+  const int qt = local / a.H, h = local - qt * a.H;
+  const int hk = h / (a.H / a.Hkv);
+  const int n = sq.len, i0 = qt * kRTile;
+  const int n_kt = (n + kRTile - 1) / kRTile;
+  const int kt0 = a.pos ? 0 : qt;                 // first key tile with an allowed key
+  const int nk = n_kt - kt0;
+  const int64_t row0 = (int64_t)layer * a.T + sq.tok_off;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ms->qfull), 1);
+    for (int i = 0; i < kRStages; ++i) {
+      mbar_init(smem_u32(&ms->full[i]), 1);
+      mbar_init(smem_u32(&ms->empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ms->s_full[b]), 1);
+      mbar_init(smem_u32(&ms->s_free[b]), 4);
+    }
+    mbar_init(smem_u32(&ms->p_full), 4);
+    mbar_init(smem_u32(&ms->p_free), 1);
+    mbar_init(smem_u32(&ms->o_done), 1);
+    mbar_init(smem_u32(&ms->drain), 1);
+    ms->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ms->tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ms->tmem_base;      // S0: columns 0..127, S1: 128..255, O: 256..383
+  uint32_t armed = 0, armed_par = 0;
+  bool q_armed = false, mma_issued = false;
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+      const uint32_t qbar = smem_u32(&ms->qfull);
+      mbar_expect_tx(qbar, kRTileBytes);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(smem_u32(s_q + hf * kRAtom), &R.tmq, qbar, hf * 64, h, (int)(row0 + i0), pol_q);
+      q_armed = true;
+      int stage = 0;
+      uint32_t phase = 0;
+      auto load = [&](const CUtensorMap* map, int kt) {
+        if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) return false;
+        const uint32_t bar = smem_u32(&ms->full[stage]);
+        mbar_expect_tx(bar, kRTileBytes);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(smem_u32(s_r + stage * kRTileBytes + hf * kRAtom), map, bar, hf * 64, hk,
+                      (int)(row0 + (int64_t)kt * kRTile), pol_kv);
+        armed |= 1u << stage;
+        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == kRStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; ok && t < nk; ++t) ok = load(&R.tmk, kt0 + t);         // pass 1
+      if (ok) ok = load(&R.tmk, kt0);                                         // pass 2
+      for (int t = 0; ok && t < nk; ++t) {
+        if (t + 1 < nk) ok = load(&R.tmk, kt0 + t + 1);
+        if (ok) ok = load(&R.tmv, kt0 + t);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(a.status, KVSEL_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = instr_desc(kRTile, kRTile);                 // S: K-major A, B
+      constexpr uint32_t kIdPV = instr_desc(kRD, kRTile) | (1u << 16);      // O: B (V) MN-major
+      const uint32_t q_addr = smem_u32(s_q), r_addr = smem_u32(s_r), p_addr = smem_u32(s_p);
+      int stage = 0, u = 0;
+      uint32_t phase = 0;
+      bool ok = mbar_wait(smem_u32(&ms->qfull), 0, limit, abort_flag);
+      auto next_stage = [&]() {
+        if (++stage == kRStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      };
+      auto issue_s = [&]() {                     // S number u from the K tile in the ring
+        const int b = u & 1;
+        if (!mbar_wait(smem_u32(&ms->s_free[b]), ((uint32_t)(u >> 1) & 1) ^ 1, limit, abort_flag) ||
+            !mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t kb = r_addr + stage * kRTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kRD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kRAtom + (kk & 3) * 32;
+          tc_mma(tmem_base + (uint32_t)(b * kRTile), smem_desc(q_addr + off), smem_desc(kb + off),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_issued = true;
+        tc_commit(smem_u32(&ms->empty[stage]));
+        tc_commit(smem_u32(&ms->s_full[b]));
+        next_stage();
+        ++u;
+        return true;
+      };
+      for (int t = 0; ok && t < nk; ++t) ok = issue_s();                     // pass 1
+      if (ok) ok = issue_s();                                                 // pass 2: S(0)
+      for (int t = 0; ok && t < nk; ++t) {
+        if (t + 1 < nk && !(ok = issue_s())) break;                           // S(t + 1)
+        // O += P(t) V(t), hi then lo
+        if (!mbar_wait(smem_u32(&ms->p_full), (uint32_t)t & 1, limit, abort_flag) ||
+            !mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = r_addr + stage * kRTileBytes;
+#pragma unroll
+        for (int which = 0; which < 2; ++which)
+#pragma unroll
+          for (int kk = 0; kk < kRTile / 16; ++kk) {
+            const uint32_t pa = p_addr + which * kRTileBytes + (kk >> 2) * kRAtom + (kk & 3) * 32;
+            tc_mma(tmem_base + 2 * kRTile, smem_desc(pa), smem_desc_mn(vb + kk * 2048), kIdPV,
+                   (t > 0 || which > 0 || kk > 0) ? 1u : 0u);
+          }
+        tc_commit(smem_u32(&ms->empty[stage]));
+        tc_commit(smem_u32(&ms->p_free));
+        next_stage();
+      }
+      if (ok) {
+        tc_commit(smem_u32(&ms->o_done));
+      } else {
+        *abort_flag = 1;
+        record_status(a.status, KVSEL_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ---- softmax warps: row r = lane quarter * 32 + lane, query i = i0 + r
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane, i = i0 + r;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const float c2 = 1.4426950408889634f / sqrtf((float)kRD);
+    const int pos_i = i < n ? (a.pos ? __ldg(a.pos + sq.tok_off + i) : i) : 0;
+    auto allowed = [&](int j) {
+      return i < n && j < n && (a.pos ? __ldg(a.pos + sq.tok_off + j) > pos_i : j > i);
+    };
+    float m = -INFINITY, l = 0.f;
+    int u = 0;
+    bool ok = true;
+    auto wait_s = [&]() {
+      const bool w = mbar_wait(smem_u32(&ms->s_full[u & 1]), (uint32_t)(u >> 1) & 1, limit,
+                               abort_flag);
+      return __all_sync(0xffffffffu, w);
+    };
+    // pass 1: row max and sum (base 2)
+    for (int t = 0; ok && t < nk; ++t) {
+      if (!(ok = wait_s())) break;
+      tc_fence_after();
+      const int j0 = (kt0 + t) * kRTile;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kRTile; c0 += 32) {
+        float x[32];
+        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + c0), x);
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          x[e] = allowed(j0 + c0 + e) ? x[e] * c2 : -INFINITY;
+          cmax = fmaxf(cmax, x[e]);
+        }
+        if (cmax > -INFINITY) {
+          if (cmax > m) {
+            l *= ex2(m - cmax);
+            m = cmax;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) l += ex2(x[e] - m);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
+      ++u;
+    }
+    if (m != -INFINITY && (!finite_f(m) || !finite_f(l))) record_status(a.status, KVSEL_ERR_NONFINITE);
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    // pass 2: P (hi, lo) into shared memory, one 16-byte chunk per 8 keys
+    for (int t = 0; ok && t < nk; ++t) {
+      if (!(ok = wait_s())) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->p_free), ((uint32_t)t & 1) ^ 1, limit,
+                                             abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int j0 = (kt0 + t) * kRTile;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kRTile; c0 += 32) {
+        float x[32];
+        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + c0), x);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int c = c0 + g * 8 + e;
+            const float p0 = allowed(j0 + c) ? ex2(x[g * 8 + e] * c2 - m) * inv_l : 0.f;
+            const float p1 = allowed(j0 + c + 1) ? ex2(x[g * 8 + e + 1] * c2 - m) * inv_l : 0.f;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
+            hi[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+            lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+          const int c = c0 + g * 8;
+          const uint32_t off = (uint32_t)((c >> 6) * kRAtom + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4*>(s_p + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(s_p + kRTileBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      tc_fence_before();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ms->s_free[u & 1]));
+        mbar_arrive(smem_u32(&ms->p_full));
+      }
+      ++u;
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->o_done), 0, limit, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      float* out = a.out + ((row0 + i) * a.H + h) * kRD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kRD; c0 += 32) {
+        float o[32];
+        tmem_load_cols<32>(lane_base + (uint32_t)(2 * kRTile + c0), o);
+        if (i < n) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(out + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        }
+      }
+      if (i < n && a.lse)
+        a.lse[((int64_t)layer * a.H + h) * a.T + sq.tok_off + i] =
+            l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    } else {
+      *abort_flag = 1;
+      record_status(a.status, KVSEL_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (ms->abort_flag) {
+    if (warp == 0 && lane == 0) {
+      if (q_armed) mbar_wait(smem_u32(&ms->qfull), 0, limit, nullptr);
+      for (int s = 0; s < kRStages; ++s)
+        if (armed & (1u << s))
+          mbar_wait(smem_u32(&ms->full[s]), (armed_par >> s) & 1, limit, nullptr);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+      tc_commit(smem_u32(&ms->drain));
+      mbar_wait(smem_u32(&ms->drain), 0, limit, nullptr);
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512)
+                 : "memory");
+  }
+}
+
+constexpr size_t reverse_smem() {
+  return 1024 + (1 + kRStages + 2) * (size_t)kRTileBytes + sizeof(RevSmem);
+}
+
+}  // namespace
+
+bool reverse_eligible(int dtype, int D, const void* q, const void* k, const void* v) {
+  if (dtype != KVSEL_BF16 || D != kRD) return false;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v)) & 15)
+    return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_reverse(const RevArgs& a) {
+  const int64_t rows = (int64_t)a.layers * a.T;
+  if (rows >= 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (a.layers * a.items_per_layer == 0) return cudaSuccess;
+  RevParams rp;
+  std::memset(&rp, 0, sizeof(rp));
+  if (!make_rows_map(&rp.tmq, a.q, kRD, a.H, rows, 1, kRTile) ||
+      !make_rows_map(&rp.tmk, a.k, kRD, a.Hkv, rows, 1, kRTile) ||
+      !make_rows_map(&rp.tmv, a.v, kRD, a.Hkv, rows, 1, kRTile))
+    return cudaErrorInvalidValue;
+  rp.a = a;
+  const size_t smem = reverse_smem();
+  cudaError_t e = cudaFuncSetAttribute(reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e) return e;
+  reverse_kernel<<<(unsigned)(a.layers * a.items_per_layer), kRThreads, smem, a.stream>>>(rp);
+  return cudaGetLastError();
+}
+
+}  // namespace kvsel

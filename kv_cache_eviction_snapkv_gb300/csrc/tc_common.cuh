@@ -134,6 +134,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return d;
 }
 
+// Shared-memory descriptor of a 128-token x 128-dimension bf16 tile read
+// MN-major (dimensions as M or N, tokens as K), 128-byte swizzle as TMA
+// writes it with 64-element boxes: 64 dimensions per 128-byte row, the next 64
+// in the other 16 KiB atom (leading byte offset), the next 8 tokens 1 KiB on
+// (stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16384 >> 4) << 16;   // LBO
+  d |= (uint64_t)(1024 >> 4) << 32;    // SBO
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: D fp32, A and B bf16, both K-major, N and M.
 __host__ __device__ constexpr uint32_t instr_desc(int n, int m) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
@@ -290,6 +305,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
   return fn;
+}
+
+// A bf16 tensor [d2][d1][d0] (d0 contiguous) as a 3-D TMA map whose box is
+// 64 x box1 x box2 elements with 128-byte swizzle (two boxes cover d0 = 128).
+bool make_rows_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint32_t box1, uint32_t box2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

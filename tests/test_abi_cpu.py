@@ -184,3 +184,28 @@ def test_jacap_host_rules(lib):
                                  None) == 2                      # grouped K/V heads
     assert lib.kvsel_jacap(ctypes.byref(sh.c), p, p, p, 8, 8, f(10), f(0.9), f(1e-6), p, p, p,
                            None) == 1                            # C <= W
+
+
+def test_reverse_host_rules(lib):
+    """Reverse-mask attention: argument rules and the tensor-path limits, on the host."""
+    from kv_cache_eviction_snapkv_gb300 import api
+    p = ctypes.c_void_p(256)
+    sh = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 300, 301], num_kv_heads=2)
+    assert lib.kvsel_reverse_attention(ctypes.byref(sh.c), None, p, p, None, p, None,
+                                       None) == 1                  # Q missing
+    assert lib.kvsel_reverse_attention(ctypes.byref(sh.c), p, p, p, None, None, None,
+                                       None) == 1                  # out missing
+    assert lib.kvsel_reverse_attention(ctypes.byref(sh.c), p, p, p, None, ctypes.c_void_p(260),
+                                       None, None) == 1            # out misaligned
+    d64 = api.Shape(1, 4, 64, api.KVSEL_BF16, [0, 300])
+    assert lib.kvsel_reverse_attention(ctypes.byref(d64.c), p, p, p, None, p, None,
+                                       None) == 2                  # D = 64
+    f32 = api.Shape(1, 4, 128, api.KVSEL_F32, [0, 300])
+    assert lib.kvsel_reverse_attention(ctypes.byref(f32.c), p, p, p, None, p, None,
+                                       None) == 2                  # fp32
+    bad = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 300, 200])
+    assert lib.kvsel_reverse_attention(ctypes.byref(bad.c), p, p, p, None, p, None,
+                                       None) == 1                  # decreasing offsets
+    empty = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 0])
+    assert lib.kvsel_reverse_attention(ctypes.byref(empty.c), None, None, None, None, None, None,
+                                       None) == 0                  # nothing to do
