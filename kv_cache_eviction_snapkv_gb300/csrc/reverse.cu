@@ -10,8 +10,9 @@
 // follows the rows' positions when they are given).
 //
 // One CTA per 128 query rows of one (layer, sequence, query head); bf16,
-// D = 128; 192 threads: warp 0 TMA, warp 1 MMA, warps 2..5 softmax (one query
-// row per thread, TMEM lane quarter warp % 4).
+// D = 128; 320 threads: warp 0 TMA, warp 1 MMA, warps 2..9 softmax (query row
+// = TMEM lane: lane quarter warp % 4; the two warps of a quarter take one
+// half of the 128 columns each, and merge their row statistics after pass 1).
 //   pass 1  S = Q K^T per 128-key tile (tcgen05, M = 128 queries, N = 128
 //           keys, K = D; two TMEM S buffers so the next tile's MMAs overlap
 //           this tile's softmax), then per row the max m and the sum l of
@@ -41,7 +42,8 @@ constexpr int kRTile = 128;                       // query rows and keys per til
 constexpr int kRTileBytes = kRTile * kRD * 2;     // one bf16 tile: 32 KiB
 constexpr int kRAtom = kRTile * 128;              // one 64-column swizzle atom: 16 KiB
 constexpr int kRStages = 3;                       // K / V ring
-constexpr int kRThreads = 192;
+constexpr int kRThreads = 320;
+constexpr int kRSoft = 256;                       // softmax threads (8 warps)
 
 struct RevSmem {
   unsigned long long qfull;
@@ -52,6 +54,7 @@ struct RevSmem {
   unsigned long long drain;                       // abort path: the MMA issuer's last commit
   uint32_t tmem_base;
   int abort_flag;
+  float half_m[2][kRTile], half_l[2][kRTile];    // pass-1 row statistics of each column half
 };
 
 struct RevParams {
@@ -61,6 +64,9 @@ struct RevParams {
   RevArgs a;
 };
 
+// kPos: the rows carry explicit positions (every key tile is visited and the
+// mask compares positions); otherwise the row order is the position order.
+template <bool kPos>
 __global__ void __launch_bounds__(kRThreads, 1)
 reverse_kernel(const __grid_constant__ RevParams R) {
   const RevArgs& a = R.a;
@@ -84,7 +90,7 @@ reverse_kernel(const __grid_constant__ RevParams R) {
   const int hk = h / (a.H / a.Hkv);
   const int n = sq.len, i0 = qt * kRTile;
   const int n_kt = (n + kRTile - 1) / kRTile;
-  const int kt0 = a.pos ? 0 : qt;                 // first key tile with an allowed key
+  const int kt0 = kPos ? 0 : qt;                  // first key tile with an allowed key
   const int nk = n_kt - kt0;
   const int64_t row0 = (int64_t)layer * a.T + sq.tok_off;
 
@@ -96,9 +102,9 @@ reverse_kernel(const __grid_constant__ RevParams R) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ms->s_full[b]), 1);
-      mbar_init(smem_u32(&ms->s_free[b]), 4);
+      mbar_init(smem_u32(&ms->s_free[b]), kRSoft / 32);
     }
-    mbar_init(smem_u32(&ms->p_full), 4);
+    mbar_init(smem_u32(&ms->p_full), kRSoft / 32);
     mbar_init(smem_u32(&ms->p_free), 1);
     mbar_init(smem_u32(&ms->o_done), 1);
     mbar_init(smem_u32(&ms->drain), 1);
@@ -227,15 +233,19 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       }
     }
   } else {
-    // ---- softmax warps: row r = lane quarter * 32 + lane, query i = i0 + r
-    const int quarter = warp & 3;
+    // ---- softmax warps: row r = lane quarter * 32 + lane, query i = i0 + r;
+    // columns cb .. cb + 63 of every tile (and of O)
+    const int quarter = warp & 3, half = (warp - 2) >> 2, cb = half * 64;
     const int r = quarter * 32 + lane, i = i0 + r;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const float c2 = 1.4426950408889634f / sqrtf((float)kRD);
-    const int pos_i = i < n ? (a.pos ? __ldg(a.pos + sq.tok_off + i) : i) : 0;
-    auto allowed = [&](int j) {
-      return i < n && j < n && (a.pos ? __ldg(a.pos + sq.tok_off + j) > pos_i : j > i);
+    const bool row_ok = i < n;
+    const int pos_i = kPos ? __ldg(a.pos + sq.tok_off + min(i, n - 1)) : i;
+    auto allowed = [&](int j) -> bool {      // branch-free: j in the sequence and later than i
+      if (kPos) return row_ok & (j < n) & (__ldg(a.pos + sq.tok_off + min(j, n - 1)) > pos_i);
+      return row_ok & (j < n) & (j > i);
     };
+    auto bar_soft = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kRSoft) : "memory"); };
     float m = -INFINITY, l = 0.f;
     int u = 0;
     bool ok = true;
@@ -244,92 +254,112 @@ reverse_kernel(const __grid_constant__ RevParams R) {
                                abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-    // pass 1: row max and sum (base 2)
+    // pass 1: this half's row max and sum (base 2)
     for (int t = 0; ok && t < nk; ++t) {
       if (!(ok = wait_s())) break;
       tc_fence_after();
-      const int j0 = (kt0 + t) * kRTile;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kRTile; c0 += 32) {
-        float x[32];
-        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + c0), x);
-        float cmax = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          x[e] = allowed(j0 + c0 + e) ? x[e] * c2 : -INFINITY;
-          cmax = fmaxf(cmax, x[e]);
-        }
-        if (cmax > -INFINITY) {
-          if (cmax > m) {
-            l *= ex2(m - cmax);
-            m = cmax;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) l += ex2(x[e] - m);
-        }
-      }
+      const int j0 = (kt0 + t) * kRTile + cb;
+      float x[64];
+      tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb), *reinterpret_cast<float(*)[32]>(x));
+      tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb + 32),
+                         *reinterpret_cast<float(*)[32]>(x + 32));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
       ++u;
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        x[e] = allowed(j0 + e) ? x[e] * c2 : -INFINITY;
+        cmax = fmaxf(cmax, x[e]);
+      }
+      if (cmax > -INFINITY) {
+        if (cmax > m) {
+          l *= ex2(m - cmax);
+          m = cmax;
+        }
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          s0 += ex2(x[e] - m);
+          s1 += ex2(x[e + 1] - m);
+        }
+        l += s0 + s1;
+      }
     }
-    if (m != -INFINITY && (!finite_f(m) || !finite_f(l))) record_status(a.status, KVSEL_ERR_NONFINITE);
+    // the two halves' statistics, merged in half order (the same in both)
+    if (ok) {
+      ms->half_m[half][r] = m;
+      ms->half_l[half][r] = l;
+    }
+    bar_soft();
+    if (ok) {
+      const float m0 = ms->half_m[0][r], l0 = ms->half_l[0][r];
+      const float m1 = ms->half_m[1][r], l1 = ms->half_l[1][r];
+      m = fmaxf(m0, m1);
+      l = m == -INFINITY ? 0.f
+                         : (m0 == -INFINITY ? 0.f : l0 * ex2(m0 - m)) +
+                               (m1 == -INFINITY ? 0.f : l1 * ex2(m1 - m));
+      if (half == 0 && m != -INFINITY && (!finite_f(m) || !finite_f(l)))
+        record_status(a.status, KVSEL_ERR_NONFINITE);
+    }
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
-    // pass 2: P (hi, lo) into shared memory, one 16-byte chunk per 8 keys
+    // pass 2: P (hi, lo) of this half in registers, then into shared memory
+    // once the previous P V has read it (atom `half` of each P buffer)
     for (int t = 0; ok && t < nk; ++t) {
       if (!(ok = wait_s())) break;
+      tc_fence_after();
+      const int j0 = (kt0 + t) * kRTile + cb;
+      uint32_t hw[32], lw[32];
+      {
+        float x[64];
+        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb), *reinterpret_cast<float(*)[32]>(x));
+        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb + 32),
+                           *reinterpret_cast<float(*)[32]>(x + 32));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float e0 = ex2(x[e] * c2 - m) * inv_l, e1 = ex2(x[e + 1] * c2 - m) * inv_l;
+          const float p0 = allowed(j0 + e) ? e0 : 0.f, p1 = allowed(j0 + e + 1) ? e1 : 0.f;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
+          hw[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+          lw[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->p_free), ((uint32_t)t & 1) ^ 1, limit,
                                              abort_flag));
       if (!ok) break;
-      tc_fence_after();
-      const int j0 = (kt0 + t) * kRTile;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kRTile; c0 += 32) {
-        float x[32];
-        tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + c0), x);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int c = c0 + g * 8 + e;
-            const float p0 = allowed(j0 + c) ? ex2(x[g * 8 + e] * c2 - m) * inv_l : 0.f;
-            const float p1 = allowed(j0 + c + 1) ? ex2(x[g * 8 + e + 1] * c2 - m) * inv_l : 0.f;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
-            hi[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
-            lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
-          }
-          const int c = c0 + g * 8;
-          const uint32_t off = (uint32_t)((c >> 6) * kRAtom + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
-          *reinterpret_cast<uint4*>(s_p + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(s_p + kRTileBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+      for (int g = 0; g < 8; ++g) {                  // 16-byte chunk g of the row in atom `half`
+        const uint32_t off = (uint32_t)(half * kRAtom + r * 128 + ((g ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(s_p + off) =
+            make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]);
+        *reinterpret_cast<uint4*>(s_p + kRTileBytes + off) =
+            make_uint4(lw[4 * g], lw[4 * g + 1], lw[4 * g + 2], lw[4 * g + 3]);
       }
-      tc_fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ms->s_free[u & 1]));
-        mbar_arrive(smem_u32(&ms->p_full));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&ms->p_full));
       ++u;
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->o_done), 0, limit, abort_flag));
     if (ok) {
       tc_fence_after();
-      float* out = a.out + ((row0 + i) * a.H + h) * kRD;
+      float* out = a.out + ((row0 + i) * a.H + h) * kRD + cb;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kRD; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         float o[32];
-        tmem_load_cols<32>(lane_base + (uint32_t)(2 * kRTile + c0), o);
-        if (i < n) {
+        tmem_load_cols<32>(lane_base + (uint32_t)(2 * kRTile + cb + c0), o);
+        if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(out + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
       }
-      if (i < n && a.lse)
+      if (row_ok && half == 0 && a.lse)
         a.lse[((int64_t)layer * a.H + h) * a.T + sq.tok_off + i] =
             l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
     } else {
@@ -386,10 +416,10 @@ cudaError_t launch_reverse(const RevArgs& a) {
     return cudaErrorInvalidValue;
   rp.a = a;
   const size_t smem = reverse_smem();
-  cudaError_t e = cudaFuncSetAttribute(reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const auto kern = a.pos ? reverse_kernel<true> : reverse_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
-  reverse_kernel<<<(unsigned)(a.layers * a.items_per_layer), kRThreads, smem, a.stream>>>(rp);
+  kern<<<(unsigned)(a.layers * a.items_per_layer), kRThreads, smem, a.stream>>>(rp);
   return cudaGetLastError();
 }
 
