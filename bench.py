@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--no-decode", action="store_true",
                    help="skip the decode-consumer measurement")
     p.add_argument("--no-jacap", action="store_true", help="skip the Jacap measurement")
+    p.add_argument("--no-reverse", action="store_true",
+                   help="skip the reverse-mask attention measurement")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-steps", type=int, default=40)
     p.add_argument("--layers", type=int, default=0,
@@ -349,6 +351,48 @@ def measure_jacap(api, wl, q_win, k, v, dev, peak, peak_kind, iters=10):
             "fused_ms": ms_full, "fused_head_tokens_per_s": wl.head_tokens() / (ms_full * 1e-3)}
 
 
+def measure_reverse(api, dev, iters=10):
+    """Reverse-mask attention of the counter-causal scorer on the shape the
+    page times (one sequence of n cached rows, 28 query heads over 4 K/V heads,
+    D = 128, bf16): one layer (the single-layer approximation) at n = 512 and
+    n = 4096, and 28 layers at n = 4096 (the attention of the full reverse
+    pass). Useful flops: QK^T and PV over the allowed pairs, 4 D n (n - 1) / 2
+    per head; peak: the measured bf16 GEMM burst rate."""
+    import torch
+    from kv_cache_eviction_snapkv_gb300 import workloads as wk
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_tf, peak_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        peak_tf, peak_kind = 1900.0, "fallback"
+    res = {"kernel": "reverse_kernel (tcgen05, two passes, P as bf16 hi + lo)",
+           "heads": 28, "kv_heads": 4, "dim": 128, "peak_tflops": peak_tf, "peak_source": peak_kind,
+           "runs": []}
+    for layers, n, it in ((1, 512, 4 * iters), (1, 4096, iters), (28, 4096, max(2, iters // 4))):
+        q, k, v = wk.reverse_tensors(layers, n, 28, 4, 128, 2000 + n, dev)
+        out = torch.empty((layers, n, 28, 128), dtype=torch.float32, device=dev)
+        lse = torch.empty((layers, 28, n), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            api.kvsel_reverse_attention(q, k, v, [0, n], out=out, lse=lse)
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(it):
+            api.kvsel_reverse_attention(q, k, v, [0, n], out=out, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / it
+        st = api.kvsel_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after reverse attention: {api.kvsel_status_string(st)}")
+        tf = layers * 28 * 4 * 128 * n * (n - 1) / 2 / (ms * 1e-3) / 1e12
+        res["runs"].append({"layers": layers, "n": n, "ms": ms, "useful_tflops": tf,
+                            "frac": tf / peak_tf})
+        del q, k, v, out, lse
+    return res
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -457,6 +501,11 @@ def main():
     if not args.no_jacap and wl.dtype == "bf16" and wl.dim == 128:
         jacap = measure_jacap(api, wl, q, k, v, dev, peak, peak_kind)
 
+    # Reverse-mask attention of the counter-causal scorer (its own inputs).
+    reverse = None
+    if not args.no_reverse and rank == 0:
+        reverse = measure_reverse(api, dev)
+
     # End to end through the C ABI with host buffers: kvsel_snapkv_host copies
     # q_win and K to the device layer by layer and reads the kept V rows and
     # writes the outputs in place in pinned host memory.
@@ -533,6 +582,7 @@ def main():
             "e2e": e2e,
             "decode": decode,
             "jacap": jacap,
+            "reverse": reverse,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

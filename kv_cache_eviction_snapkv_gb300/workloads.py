@@ -407,6 +407,19 @@ def device_tensors(wl: Workload, device, chunk: int = 1 << 26):
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 
+def reverse_tensors(layers: int, n: int, heads: int, kv_heads: int, dim: int, seed: int,
+                    device):
+    """Inputs of the reverse-mask attention: Q [layers, n, heads, dim] and K, V
+    [layers, n, kv_heads, dim], bf16 N(0,1) quantiles from the counter-based
+    generator (one sequence of n cached rows; Q and K/V from two streams)."""
+    wq = custom_workload("reverse_q", layers, heads, dim, n, n + 1, "bf16", "avg", 1, [n], seed)
+    wkv = custom_workload("reverse_kv", layers, kv_heads, dim, 1, n + 1, "bf16", "avg", 1, [n],
+                          seed + 7919)
+    q = device_tensors(wq, device)[0]
+    _, k, v = device_tensors(wkv, device)
+    return q, k, v
+
+
 def storage_to_torch(x: np.ndarray, dtype: str):
     """numpy storage array -> CPU torch tensor of the storage dtype (no copy of bits)."""
     import torch
