@@ -220,13 +220,17 @@ class ClockSampler:
 def score_traffic(layers_full: int):
     """DRAM bytes per full launch of the scoring kernel from the committed ncu
     summary, scaled from the captured layer count; None when the kernel source
-    changed since the capture (its sha256 is recorded beside the counters)."""
+    (score_tc.cu and tc_common.cuh) changed since the capture (their sha256 is
+    recorded beside the counters)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "score_tc_cfg2_ncu.md")
-    src = os.path.join(ROOT, "kv_cache_eviction_snapkv_gb300", "csrc", "score_tc.cu")
+    csrc = os.path.join(ROOT, "kv_cache_eviction_snapkv_gb300", "csrc")
     try:
         text = open(path).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for name in ("score_tc.cu", "tc_common.cuh"):      # the kernel and its helpers
+            h.update(open(os.path.join(csrc, name), "rb").read())
+        digest = h.hexdigest()
     except OSError:
         return None
     fields = dict(line.split(":", 1) for line in text.splitlines()
