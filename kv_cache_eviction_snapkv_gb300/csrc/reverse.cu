@@ -15,13 +15,14 @@
 // half of the 128 columns each, and merge their row statistics after pass 1).
 //   pass 1  S = Q K^T per 128-key tile (tcgen05, M = 128 queries, N = 128
 //           keys, K = D; two TMEM S buffers so the next tile's MMAs overlap
-//           this tile's softmax), then per row the max m and the sum l of
-//           2^x, x = S log2(e) / sqrt(D), over the allowed keys;
-//   pass 2  S again; P = 2^(x - m) / l in fp32 for the allowed keys (0
-//           elsewhere), split into bf16 hi = bf16(P) and lo = bf16(P - hi),
-//           written K-major (keys as K) to shared memory; O += P_hi V + P_lo V
-//           (tcgen05, V read MN-major as TMA wrote it), O in TMEM; at the end
-//           O (already normalised) and lse = (m + log2 l) ln 2 are written.
+//           this tile's softmax), then per row the maximum of S over the
+//           allowed keys, m = max S log2(e) / sqrt(D);
+//   pass 2  S again; P = 2^(x - m), x = S log2(e) / sqrt(D), in fp32 for the
+//           allowed keys (0 elsewhere; P <= 1), summed into l and split into
+//           bf16 hi = bf16(P) and lo = bf16(P - hi), written K-major (keys as
+//           K) to shared memory; O += P_hi V + P_lo V (tcgen05, V read
+//           MN-major as TMA wrote it), O in TMEM; at the end O / l and
+//           lse = (m + log2 l) ln 2 are written.
 // The producer loads in the order the MMA issuer consumes: pass 1 K tiles,
 // then K(0), and per tile t: K(t + 1), V(t) (S(t + 1) is issued before
 // P(t) V(t)). With positions in row order, key tiles before the query tile
@@ -246,6 +247,9 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       return row_ok & (j < n) & (j > i);
     };
     auto bar_soft = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kRSoft) : "memory"); };
+    // a tile whose keys all lie after every query row of the tile and inside
+    // the sequence needs no mask (the same answer in every thread)
+    auto tile_full = [&](int jt) { return !kPos && jt > i0 + kRTile - 1 && jt + kRTile <= n; };
     float m = -INFINITY, l = 0.f;
     int u = 0;
     bool ok = true;
@@ -254,11 +258,12 @@ reverse_kernel(const __grid_constant__ RevParams R) {
                                abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-    // pass 1: this half's row max and sum (base 2)
+    // pass 1: this half's row maximum of the raw logits q . k over the allowed keys
+    float smax = -INFINITY;
     for (int t = 0; ok && t < nk; ++t) {
       if (!(ok = wait_s())) break;
       tc_fence_after();
-      const int j0 = (kt0 + t) * kRTile + cb;
+      const int jt = (kt0 + t) * kRTile, j0 = jt + cb;
       float x[64];
       tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb), *reinterpret_cast<float(*)[32]>(x));
       tmem_load_cols<32>(lane_base + (uint32_t)((u & 1) * kRTile + cb + 32),
@@ -267,49 +272,25 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
       ++u;
-      float cmax = -INFINITY;
+      if (tile_full(jt)) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        x[e] = allowed(j0 + e) ? x[e] * c2 : -INFINITY;
-        cmax = fmaxf(cmax, x[e]);
-      }
-      if (cmax > -INFINITY) {
-        if (cmax > m) {
-          l *= ex2(m - cmax);
-          m = cmax;
-        }
-        float s0 = 0.f, s1 = 0.f;
+        for (int e = 0; e < 64; ++e) smax = fmaxf(smax, x[e]);
+      } else {
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          s0 += ex2(x[e] - m);
-          s1 += ex2(x[e + 1] - m);
-        }
-        l += s0 + s1;
+        for (int e = 0; e < 64; ++e) smax = fmaxf(smax, allowed(j0 + e) ? x[e] : -INFINITY);
       }
     }
-    // the two halves' statistics, merged in half order (the same in both)
-    if (ok) {
-      ms->half_m[half][r] = m;
-      ms->half_l[half][r] = l;
-    }
+    // the row maximum in base-2 units, from both halves
+    if (ok) ms->half_m[half][r] = smax * c2;
     bar_soft();
-    if (ok) {
-      const float m0 = ms->half_m[0][r], l0 = ms->half_l[0][r];
-      const float m1 = ms->half_m[1][r], l1 = ms->half_l[1][r];
-      m = fmaxf(m0, m1);
-      l = m == -INFINITY ? 0.f
-                         : (m0 == -INFINITY ? 0.f : l0 * ex2(m0 - m)) +
-                               (m1 == -INFINITY ? 0.f : l1 * ex2(m1 - m));
-      if (half == 0 && m != -INFINITY && (!finite_f(m) || !finite_f(l)))
-        record_status(a.status, KVSEL_ERR_NONFINITE);
-    }
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    if (ok) m = fmaxf(ms->half_m[0][r], ms->half_m[1][r]);
     // pass 2: P (hi, lo) of this half in registers, then into shared memory
     // once the previous P V has read it (atom `half` of each P buffer)
     for (int t = 0; ok && t < nk; ++t) {
       if (!(ok = wait_s())) break;
       tc_fence_after();
-      const int j0 = (kt0 + t) * kRTile + cb;
+      const int jt = (kt0 + t) * kRTile, j0 = jt + cb;
+      const bool full = tile_full(jt);
       uint32_t hw[32], lw[32];
       {
         float x[64];
@@ -321,8 +302,10 @@ reverse_kernel(const __grid_constant__ RevParams R) {
         if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const float e0 = ex2(x[e] * c2 - m) * inv_l, e1 = ex2(x[e + 1] * c2 - m) * inv_l;
-          const float p0 = allowed(j0 + e) ? e0 : 0.f, p1 = allowed(j0 + e + 1) ? e1 : 0.f;
+          const float e0 = ex2(fmaf(x[e], c2, -m)), e1 = ex2(fmaf(x[e + 1], c2, -m));
+          const float p0 = full || allowed(j0 + e) ? e0 : 0.f;
+          const float p1 = full || allowed(j0 + e + 1) ? e1 : 0.f;
+          l += p0 + p1;
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
           hw[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
@@ -345,6 +328,15 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       if (lane == 0) mbar_arrive(smem_u32(&ms->p_full));
       ++u;
     }
+    // the row sum from both halves (half order), then O / l
+    if (ok) ms->half_l[half][r] = l;
+    bar_soft();
+    if (ok) {
+      l = ms->half_l[0][r] + ms->half_l[1][r];
+      if (half == 0 && (!finite_f(l) || (m != -INFINITY && !finite_f(m))))
+        record_status(a.status, KVSEL_ERR_NONFINITE);
+    }
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->o_done), 0, limit, abort_flag));
     if (ok) {
       tc_fence_after();
@@ -356,7 +348,8 @@ reverse_kernel(const __grid_constant__ RevParams R) {
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(out + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            *reinterpret_cast<float4*>(out + c0 + e) =
+                make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l, o[e + 3] * inv_l);
         }
       }
       if (row_ok && half == 0 && a.lse)
