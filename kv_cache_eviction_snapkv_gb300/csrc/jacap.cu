@@ -621,27 +621,31 @@ constexpr int kFB = kJD / 8;                   // 8 x 8 blocks per side
 
 // One CTA per instance, 160 threads: thread tid < 136 holds the lower block
 // (bi, bk), bk <= bi, numbered row by row (tid = bi (bi + 1) / 2 + bk), in
-// registers; three CTAs fit an SM (registers and shared memory). Both phases are right-looking, one column (row) per step and
+// registers; three CTAs fit an SM (registers and shared memory). Both
+// phases take two columns (rows) per step, one barrier per step. Both phases are right-looking, one column (row) per step and
 // one barrier per step:
-//   Cholesky  step j: the owners of column j (bk = j / 8) store its current
-//             values to shared memory; every thread reads the pivot d = A[j][j]
-//             and the column, l_i = A[i][j] / sqrt(d), and updates its
-//             entries right of j by -l_i l_k. The stored columns (before
-//             scaling) and 1 / sqrt(d) are kept for the inverse.
-//   inverse   L X = I by rows: B = I; step j: X[j][:] = B[j][:] / L[j][j]
-//             (the owners of row j, bi = j / 8, scale it and store it to a
-//             double-buffered row), then every row i > j takes
-//             B[i][:] -= L[i][j] X[j][:].
+//   Cholesky  step (j, j+1), j even: the owners of the two columns (bk = j / 8)
+//             store their current values to shared memory; every thread takes
+//             the 2 x 2 pivot block (L00 = sqrt(a_jj), L10 = a_j+1,j / L00,
+//             L11 = sqrt(a_j+1,j+1 - L10^2)), the columns of L for its rows
+//             and columns (l_i0 = a_ij / L00, l_i1 = (a_i,j+1 - l_i0 L10) / L11)
+//             and updates its entries right of j + 1 by -(l_i0 l_k0 + l_i1 l_k1).
+//             The stored columns (before scaling) and (1 / L00, L10, 1 / L11)
+//             are kept for the inverse.
+//   inverse   L X = I by rows: B = I; step (j, j+1): X_j = B_j / L00 and
+//             X_j+1 = (B_j+1 - L10 X_j) / L11 (the owners of the two rows,
+//             bi = j / 8, store them to a double-buffered pair of rows), then
+//             every row i > j + 1 takes B_i -= L_ij X_j + L_i,j+1 X_j+1.
 // Entries above the diagonal of a diagonal block collect values that are
 // never read; the output writes zeros there.
 constexpr int kFThreads = 160;
 constexpr int kFBlocks = kFB * (kFB + 1) / 2;   // 136 lower blocks
 
-__global__ void __launch_bounds__(kFThreads) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
+__global__ void __launch_bounds__(kFThreads, 3) jacap_factor_kernel(const __grid_constant__ JacapArgs a) {
   extern __shared__ float4 fs4[];
-  float* Lc = reinterpret_cast<float*>(fs4);    // [kJD][kJD]: column j of the updated matrix at step j
-  __shared__ float dinv[kJD];                   // 1 / L[j][j]
-  __shared__ __align__(16) float xrow[2][kJD];  // X[j][:] of the current inverse step
+  float* Lc = reinterpret_cast<float*>(fs4);    // [kJD][kJD]: column j of the updated matrix at its step
+  __shared__ float3 piv[kJD / 2];               // (1 / L00, L10, 1 / L11) of each column pair
+  __shared__ __align__(16) float xrow[2][2][kJD];  // X rows j, j+1 of the current inverse step
   __shared__ int bad;
   const int tid = threadIdx.x;
   const bool act = tid < kFBlocks;
@@ -686,72 +690,104 @@ __global__ void __launch_bounds__(kFThreads) jacap_factor_kernel(const __grid_co
     v[4] = u1.x * s, v[5] = u1.y * s, v[6] = u1.z * s, v[7] = u1.w * s;
   };
 
-  // ---- Cholesky
+  // the pivot block of a column pair and the two columns of L at 8 rows
+  auto pivot = [&](int j, float& inv0, float& l10, float& inv1) {
+    const float pa = Lc[j * kJD + j], pb = Lc[j * kJD + j + 1], pc = Lc[(j + 1) * kJD + j + 1];
+    const float l00 = sqrtf(fmaxf(pa, 1e-30f));
+    inv0 = 1.f / l00;
+    l10 = pb * inv0;
+    const float pd = pc - l10 * l10;
+    inv1 = 1.f / sqrtf(fmaxf(pd, 1e-30f));
+    return (pa > 0.f) && finite_f(pa) && (pd > 0.f) && finite_f(pd);
+  };
+  auto lcols = [&](int j, int row0, float inv0, float l10, float inv1, float* v0, float* v1) {
+    load8(Lc + j * kJD + row0, v0, inv0);
+    float w[8];
+    load8(Lc + (j + 1) * kJD + row0, w, 1.f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v1[e] = (w[e] - v0[e] * l10) * inv1;
+  };
+
+  // ---- Cholesky, two columns per step
   for (int jb = 0; jb < kFB; ++jb) {
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = jb * 8 + jj;
+    for (int jp = 0; jp < 4; ++jp) {
+      const int jj = 2 * jp, j = jb * 8 + jj;
       if (bk == jb && bi >= jb) {
-        float4* dst = reinterpret_cast<float4*>(Lc + j * kJD + bi * 8);
-        dst[0] = make_float4(R[0][jj], R[1][jj], R[2][jj], R[3][jj]);
-        dst[1] = make_float4(R[4][jj], R[5][jj], R[6][jj], R[7][jj]);
+        float4* d0 = reinterpret_cast<float4*>(Lc + j * kJD + bi * 8);
+        float4* d1 = reinterpret_cast<float4*>(Lc + (j + 1) * kJD + bi * 8);
+        d0[0] = make_float4(R[0][jj], R[1][jj], R[2][jj], R[3][jj]);
+        d0[1] = make_float4(R[4][jj], R[5][jj], R[6][jj], R[7][jj]);
+        d1[0] = make_float4(R[0][jj + 1], R[1][jj + 1], R[2][jj + 1], R[3][jj + 1]);
+        d1[1] = make_float4(R[4][jj + 1], R[5][jj + 1], R[6][jj + 1], R[7][jj + 1]);
       }
       __syncthreads();
-      const float d = Lc[j * kJD + j];
-      const float inv = 1.f / sqrtf(fmaxf(d, 1e-30f));
+      float inv0, l10, inv1;
+      const bool good = pivot(j, inv0, l10, inv1);
       if (tid == 0) {
-        dinv[j] = inv;
-        if (!(d > 0.f) || !finite_f(d)) bad = 1;
+        piv[j >> 1] = make_float3(inv0, l10, inv1);
+        if (!good) bad = 1;
       }
       if (act && bk >= jb) {
-        float lr[8], lc[8];
-        load8(Lc + j * kJD + bi * 8, lr, inv);
-        load8(Lc + j * kJD + bk * 8, lc, inv);
+        float r0[8], r1[8], c0[8], c1[8];
+        lcols(j, bi * 8, inv0, l10, inv1, r0, r1);
+        lcols(j, bk * 8, inv0, l10, inv1, c0, c1);
         if (bk == jb) {
 #pragma unroll
           for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int c = jj + 1; c < 8; ++c) R[r][c] = fmaf(-lr[r], lc[c], R[r][c]);
+            for (int c = jj + 2; c < 8; ++c)
+              R[r][c] = fmaf(-r1[r], c1[c], fmaf(-r0[r], c0[c], R[r][c]));
         } else {
 #pragma unroll
           for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-lr[r], lc[c], R[r][c]);
+            for (int c = 0; c < 8; ++c)
+              R[r][c] = fmaf(-r1[r], c1[c], fmaf(-r0[r], c0[c], R[r][c]));
         }
       }
     }
   }
 
-  // ---- X = L^{-1}
+  // ---- X = L^{-1}, two rows per step
   set_identity();
   for (int jb = 0; jb < kFB; ++jb) {
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = jb * 8 + jj;
-      float* xr = xrow[jj & 1];
+    for (int jp = 0; jp < 4; ++jp) {
+      const int jj = 2 * jp, j = jb * 8 + jj;
+      float (*xr)[kJD] = xrow[jp & 1];
+      const float3 pv = piv[j >> 1];
       if (bi == jb && bk <= jb) {
-        const float di = dinv[j];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) R[jj][c] *= di;
-        float4* dst = reinterpret_cast<float4*>(xr + bk * 8);
-        dst[0] = make_float4(R[jj][0], R[jj][1], R[jj][2], R[jj][3]);
-        dst[1] = make_float4(R[jj][4], R[jj][5], R[jj][6], R[jj][7]);
+        for (int c = 0; c < 8; ++c) {
+          R[jj][c] *= pv.x;
+          R[jj + 1][c] = (R[jj + 1][c] - pv.y * R[jj][c]) * pv.z;
+        }
+        float4* d0 = reinterpret_cast<float4*>(xr[0] + bk * 8);
+        float4* d1 = reinterpret_cast<float4*>(xr[1] + bk * 8);
+        d0[0] = make_float4(R[jj][0], R[jj][1], R[jj][2], R[jj][3]);
+        d0[1] = make_float4(R[jj][4], R[jj][5], R[jj][6], R[jj][7]);
+        d1[0] = make_float4(R[jj + 1][0], R[jj + 1][1], R[jj + 1][2], R[jj + 1][3]);
+        d1[1] = make_float4(R[jj + 1][4], R[jj + 1][5], R[jj + 1][6], R[jj + 1][7]);
       }
       __syncthreads();
       if (bi >= jb && bk <= jb) {
-        float li[8], x[8];
-        load8(Lc + j * kJD + bi * 8, li, dinv[j]);
-        load8(xr + bk * 8, x, 1.f);
+        float l0[8], l1[8], x0[8], x1[8];
+        lcols(j, bi * 8, pv.x, pv.y, pv.z, l0, l1);
+        load8(xr[0] + bk * 8, x0, 1.f);
+        load8(xr[1] + bk * 8, x1, 1.f);
         if (bi == jb) {
 #pragma unroll
-          for (int r = jj + 1; r < 8; ++r)
+          for (int r = jj + 2; r < 8; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-li[r], x[c], R[r][c]);
+            for (int c = 0; c < 8; ++c)
+              R[r][c] = fmaf(-l1[r], x1[c], fmaf(-l0[r], x0[c], R[r][c]));
         } else {
 #pragma unroll
           for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) R[r][c] = fmaf(-li[r], x[c], R[r][c]);
+            for (int c = 0; c < 8; ++c)
+              R[r][c] = fmaf(-l1[r], x1[c], fmaf(-l0[r], x0[c], R[r][c]));
         }
       }
     }
