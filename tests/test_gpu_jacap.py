@@ -41,6 +41,7 @@ CASES = [
     ("few_instances_many_splits", 1, 2, 16, 256, [1500, 700, 3000]),
     ("two_layers_window32", 2, 3, 32, 512, [2049, 515]),
     ("short_pool", 1, 2, 8, 64, [200, 136, 9]),
+    ("window40_two_query_rounds", 1, 2, 40, 300, [1000, 299]),   # W > 32: queries staged twice
 ]
 
 
