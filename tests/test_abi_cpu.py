@@ -209,3 +209,16 @@ def test_reverse_host_rules(lib):
     empty = api.Shape(1, 4, 128, api.KVSEL_BF16, [0, 0])
     assert lib.kvsel_reverse_attention(ctypes.byref(empty.c), None, None, None, None, None, None,
                                        None) == 0                  # nothing to do
+
+
+def test_binding_arity_matches_the_header():
+    """Every declaration's parameter count equals its ctypes signature's."""
+    from kv_cache_eviction_snapkv_gb300 import _native
+    text = open(os.path.join(ROOT, "include", "kvsel.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = re.findall(r"\b(kvsel_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S)
+    assert decls
+    for name, params in decls:
+        params = " ".join(params.split())
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(_native.SIGNATURES[name][1]) == n, (name, n)
