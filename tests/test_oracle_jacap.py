@@ -115,3 +115,18 @@ def test_head_selection_structure():
     assert jc.jacap_head(q[:3], k[:10], v[:10], 20)["indices"] == list(range(10))   # bypass
     with pytest.raises(OracleArgumentError):
         jc.jacap_head(q, k, v, W)
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_leverage_bound_from_sherman_morrison(seed):
+    """A >= I + w_i u_i u_i^T, so r_i <= w_i |u_i|^2 / (1 + w_i |u_i|^2) < 1
+    (Sherman-Morrison on the rank-one term), with equality for a lone token."""
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal((50, 6))
+    w = rng.uniform(0.0, 3.0, 50)
+    r = jc.leverage(w, u)["r"]
+    q = w * np.sum(u * u, axis=1)
+    assert np.all(r >= 0.0)
+    assert np.all(r <= q / (1.0 + q) * (1 + 1e-12))
+    lone = jc.leverage(w[:1], u[:1])["r"][0]
+    assert lone == pytest.approx(q[0] / (1.0 + q[0]), rel=1e-12)
