@@ -152,3 +152,11 @@ def test_planted_mistakes_fail_a_pin():
     assert not pins_hold(*variant(lambda j, i: j >= i, 0.5))
     assert not pins_hold(*variant(lambda j, i: j < i, 0.5))
     assert not pins_hold(*variant(lambda j, i: j > i, 1.0))
+
+
+def test_outputs_are_convex_combinations_of_later_values():
+    q, k, v = _head(31, 8, 12, dv=4)
+    out, _ = rev.reverse_attention(q * 3.0, k, v)
+    for i in range(30):
+        lo, hi = v[i + 1:].min(axis=0), v[i + 1:].max(axis=0)
+        assert np.all(out[i] >= lo - 1e-12) and np.all(out[i] <= hi + 1e-12)
