@@ -148,14 +148,21 @@ kvsel_status kvsel_score(const kvsel_shape* shape, const void* q_win, const void
  * (every GPU that loads the library holds it until the process exits). The
  * first call on a device looks up that array's device address (once per
  * device, with the device current); make that first call before any stream
- * capture. Calls whose scratch need exceeds 8 MiB (roughly: layers x heads x
- * ceil(L / 1024) x W x 8 bytes summed over sequences, plus small tables)
- * return KVSEL_ERR_UNSUPPORTED and launch nothing. All calls on a device share
- * the array and each call resets what must start out empty, so calls that
- * overlap on the GPU (different streams without ordering) race. */
+ * capture. Calls whose scratch need exceeds 8 MiB return
+ * KVSEL_ERR_UNSUPPORTED and launch nothing; kvsel_score_static_bytes gives
+ * the exact need of a call. All calls on a device share the array and each
+ * call resets what must start out empty, so calls that overlap on the GPU
+ * (different streams without ordering) race. */
 kvsel_status kvsel_score_static(const kvsel_shape* shape, const void* q_win, const void* K,
                                 int32_t W, int32_t pool_kind, int32_t pool_k, float* votes,
                                 float* pooled, void* stream);
+
+/* Scratch bytes kvsel_score_static needs for this shape, window and the
+ * current device (the sequence tables, the cross-chunk statistics slots and
+ * the merged statistics of the scoring kernel it would launch; q_win and K
+ * are assumed 16-byte aligned), or -1 if the arguments break a rule of
+ * kvsel_score. At most 8 MiB is accepted. Host only. */
+int64_t kvsel_score_static_bytes(const kvsel_shape* shape, int32_t W);
 
 /* Top-(C - W) selection from given pooled scores ([num_layers][H][T] fp32,
  * only prefix entries are read) into out_idx ([num_layers][T_out][H] int32);
@@ -357,6 +364,11 @@ kvsel_status kvsel_profile_end(double* stage_ms, int32_t* calls);
  * still running on the GPU must have finished (the call synchronises each
  * device first). */
 void kvsel_release(void);
+
+/* Bytes of the internal workspace (the cudaMalloc'd scratch of every entry
+ * point but kvsel_score_static) currently held on the current device; 0
+ * before the first call that needs one and after kvsel_release. Host only. */
+int64_t kvsel_workspace_bytes(void);
 
 #ifdef __cplusplus
 }

@@ -30,6 +30,8 @@ SIGNATURES = {
     "kvsel_window_logits": (c_i32, [_P, c_vp, c_vp, c_i32, c_vp, c_vp]),
     "kvsel_score": (c_i32, [_P, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "kvsel_score_static": (c_i32, [_P, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "kvsel_score_static_bytes": (c_i64, [_P, c_i32]),
+    "kvsel_workspace_bytes": (c_i64, []),
     "kvsel_select": (c_i32, [_P, c_vp, c_i32, c_i32, c_vp, c_vp]),
     "kvsel_compact": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "kvsel_snapkv": (c_i32, [_P, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,

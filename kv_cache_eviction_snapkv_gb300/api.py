@@ -174,6 +174,12 @@ def kvsel_score_static(q_win, K, seq_offsets, W: int, pool_kind: int, pool_k: in
     return votes, pooled
 
 
+def kvsel_score_static_bytes(shape: Shape, W: int) -> int:
+    """Scratch bytes kvsel_score_static needs for this shape and window (-1: a
+    rule is broken)."""
+    return int(_native.lib().kvsel_score_static_bytes(shape.ref, int(W)))
+
+
 def kvsel_select(pooled, seq_offsets, num_heads: int, W: int, C: int, out_idx=None,
                  stream=None):
     """out_idx [layers, T_out, H] int32 from pooled scores [layers, H, T]."""
@@ -453,3 +459,8 @@ def kvsel_profile_end():
 
 def kvsel_release() -> None:
     _native.lib().kvsel_release()
+
+
+def kvsel_workspace_bytes() -> int:
+    """Bytes of the library's cudaMalloc'd workspace held on the current device."""
+    return int(_native.lib().kvsel_workspace_bytes())

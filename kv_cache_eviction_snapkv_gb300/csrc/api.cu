@@ -231,6 +231,7 @@ struct ScorePass {
   int q_row0 = 0;      // the first of them within each sequence's rows of q_win
   int vote_cut = 0;    // votes kept for tok < L - W - vote_cut of the pass's L
   int accumulate = 0;  // added to the votes of the previous pass
+  int two_pass = 0;    // > 0: the two-pass kernel with this lag (long instances)
 };
 
 struct ScorePlan {
@@ -249,6 +250,19 @@ struct ScorePlan {
 // pass's padded rows, beyond W, read as zeros, as in a single pass.) Used once
 // an instance exceeds kSplitChunks items of the 64-row kernel.
 constexpr int kSplitChunks = 64;
+
+// Long instances (more than kTwoPassChunks work items) take the two-pass
+// kernel: pass 1 of an item computes its row statistics and frees its tensor
+// memory, pass 2 recomputes the logits kTwoPassLag items later (K from L2)
+// and writes the votes, so K is read from HBM once at any window.
+#ifndef KVSEL_TWO_PASS_CHUNKS
+#define KVSEL_TWO_PASS_CHUNKS 64
+#endif
+#ifndef KVSEL_TWO_PASS_LAG
+#define KVSEL_TWO_PASS_LAG 3
+#endif
+constexpr int kTwoPassChunks = KVSEL_TWO_PASS_CHUNKS;
+constexpr int kTwoPassLag = KVSEL_TWO_PASS_LAG;
 
 kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* k,
                         const DevState* d, ScorePlan* sp, bool allow_split = true) {
@@ -283,6 +297,11 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
     // span at most three rounds of items (chunks <= 2 x CTAs)
     if (one.max_chunks <= tc_max_chunks(W, d->sm_count)) {
       sp->tc = true;
+      if (allow_split && one.max_chunks > kTwoPassChunks) {
+        one.two_pass = kTwoPassLag;
+        sp->passes.push_back(std::move(one));
+        return KVSEL_OK;
+      }
       if (allow_split && tc_window_pad(W) == 64 && one.max_chunks > kSplitChunks) {
         ScorePass a0, a1;
         a0.W = 32;
@@ -341,7 +360,6 @@ kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, D
   if (items > 0x7fffffffLL) return KVSEL_ERR_UNSUPPORTED;
   const size_t o_seq = cv.take(ps.scored.size() * sizeof(SeqDesc));
   const size_t o_part = cv.take((size_t)items * ps.wpad * 2 * sizeof(float));
-  const size_t o_cnt = cv.take((size_t)insts * 2 * sizeof(int));
   const size_t o_fin = cv.take((size_t)insts * ps.wpad * 2 * sizeof(float));
   cudaError_t e = cudaMemcpyAsync(ws + o_seq, ps.scored.data(),
                                   ps.scored.size() * sizeof(SeqDesc),
@@ -362,6 +380,7 @@ kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, D
   a.q_row0 = ps.q_row0;
   a.vote_cut = ps.vote_cut;
   a.accumulate = ps.accumulate;
+  a.two_pass = ps.two_pass;
   a.n_scored = (int)ps.scored.size();
   a.seqs = reinterpret_cast<const SeqDesc*>(ws + o_seq);
   a.items_per_layer = ps.items_per_layer;
@@ -371,8 +390,6 @@ kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, D
   a.scale = (float)(1.0 / std::sqrt((double)p.D));
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
   a.part = reinterpret_cast<float*>(ws + o_part);
-  a.counters = reinterpret_cast<int*>(ws + o_cnt);
-  a.flags = a.counters + insts;
   a.final_stats = reinterpret_cast<float*>(ws + o_fin);
   a.votes = votes;
   a.logits = logits;
@@ -419,7 +436,7 @@ size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
     const int64_t items = (int64_t)p.layers * ps.items_per_layer;
     const int64_t insts = (int64_t)p.layers * ps.inst_per_layer;
     total += ps.scored.size() * sizeof(SeqDesc) + (size_t)items * ps.wpad * 8 +
-             (size_t)insts * 8 + (size_t)insts * ps.wpad * 8 + 4 * 256;
+             (size_t)insts * ps.wpad * 8 + 3 * 256;
   }
   return total;
 }
@@ -472,7 +489,6 @@ size_t static_score_bytes(const Plan& p, const ScorePlan& sp) {
     const int64_t insts = (int64_t)p.layers * ps.inst_per_layer;
     c.take(ps.scored.size() * sizeof(SeqDesc));               // scored sequences
     c.take((size_t)items * ps.wpad * 2 * sizeof(float));      // exchange slots / partials
-    c.take((size_t)insts * 2 * sizeof(int));                  // counters
     c.take((size_t)insts * ps.wpad * 2 * sizeof(float));      // merged statistics / slots
   }
   return c.off;
@@ -481,6 +497,21 @@ size_t static_score_bytes(const Plan& p, const ScorePlan& sp) {
 }  // namespace
 
 }  // namespace kvsel
+
+extern "C" int64_t kvsel_score_static_bytes(const kvsel_shape* shape, int32_t W) {
+  using namespace kvsel;
+  Plan p;
+  if (plan_shape(shape, 0, &p) != KVSEL_OK || check_window(p, W) != KVSEL_OK) return -1;
+  DevState* d = nullptr;
+  if (device_state(&d) != KVSEL_OK) return -1;
+  ScorePlan sp;
+  // alignment is unknown here: assume 256-byte aligned tensors
+  static const char probe[512] = {0};
+  const void* aligned = reinterpret_cast<const void*>(
+      (reinterpret_cast<uintptr_t>(probe) + 255) & ~uintptr_t(255));
+  if (plan_score(p, W, 0, aligned, aligned, d, &sp) != KVSEL_OK) return -1;
+  return (int64_t)static_score_bytes(p, sp);
+}
 
 extern "C" kvsel_status kvsel_score_static(const kvsel_shape* shape, const void* q_win,
                                            const void* K, int32_t W, int32_t pool_kind,
@@ -563,11 +594,13 @@ int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C) {
   if (device_state(&d) != KVSEL_OK) return -1;
   ScorePlan sp;
   // alignment is unknown here: assume 256-byte aligned tensors
-  static const char probe[32] = {0};
+  static const char probe[512] = {0};
   const void* aligned = reinterpret_cast<const void*>(
       (reinterpret_cast<uintptr_t>(probe) + 255) & ~uintptr_t(255));
   if (plan_score(p, W, C, aligned, aligned, d, &sp) != KVSEL_OK) return -1;
-  return sp.tc ? (sp.passes.size() > 1 ? 2 : 1) : 0;
+  if (!sp.tc) return 0;
+  if (sp.passes.size() > 1) return 2;
+  return sp.passes[0].two_pass ? 3 : 1;
 }
 
 kvsel_status kvsel_window_logits(const kvsel_shape* shape, const void* q_win, const void* K,
@@ -1417,6 +1450,13 @@ void kvsel_release(void) {
     }
   }
   cudaSetDevice(cur);
+}
+
+int64_t kvsel_workspace_bytes(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return (int64_t)(g_dev[dev].ws_bytes + g_dev[dev].stage_bytes);
 }
 
 }  // extern "C"

@@ -35,6 +35,8 @@ struct ScoreArgs {
   int q_row0;              // this pass's first window row within a sequence's q_W rows
   int vote_cut;            // votes are written for tok < len - W - vote_cut, 0 elsewhere
   int accumulate;          // 1: add this pass's votes to those already in `votes`
+  int two_pass;            // > 0: the two-pass kernel for long instances (statistics,
+                           // then votes from recomputed logits this many items later)
   int n_scored;            // number of scored sequences
   const SeqDesc* seqs;     // device: the scored sequences, in order
   int items_per_layer, inst_per_layer;
@@ -43,8 +45,6 @@ struct ScoreArgs {
   float scale_log2;        // log2(e) / sqrt(D): logits in base-2 units
   float scale;             // 1 / sqrt(D): logits as the page defines them
   float* part;             // [items][Wp][2] chunk (max, sum) in base-2 units
-  int* counters;           // [instances] chunks that published their stats
-  int* flags;              // [instances] 1 once the merged stats are written
   float* final_stats;      // [instances][Wp] max + log2(sum) per window row (CUDA-core
                            // path); [instances][Wp][2] final (max, sum) slots (tensor cores)
   float* votes;            // [layers][H][T]

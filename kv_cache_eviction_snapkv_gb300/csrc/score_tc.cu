@@ -238,6 +238,268 @@ __device__ __forceinline__ void rescale_row(uint32_t base, int col, int t, float
 // The kernel
 // ---------------------------------------------------------------------------
 
+// The statistics warp of the scoring kernels: collects, for each of this
+// CTA's items in order, M_r + log2 Z_r of every row of its instance for the
+// vote pass. Where the pairs of all chunks of the instance fit the staging
+// buffer, one bulk copy brings them into shared memory (repeated until every
+// pair is published) and the warp merges each row over the chunks in chunk
+// order. Larger instances go through owners: row r is merged by chunk r mod nc
+// (same order), which publishes the instance's final pair of that row; every
+// chunk then reads the W final pairs. The owner step runs ahead of the
+// collection step; each turn of the loop issues its loads together.
+template <int NW>
+__device__ __forceinline__ void stats_warp_loop(const ScoreArgs& a, Misc* ms, int n_my, int G,
+                                                int lane, unsigned long long limit,
+                                                volatile int* abort_flag) {
+  const int W = a.W;
+  constexpr int kStageSlots = slot_stage_for(NW) / 16;   // per staging buffer
+  const unsigned long long* part = reinterpret_cast<const unsigned long long*>(a.part);
+  unsigned long long* fslots = reinterpret_cast<unsigned long long*>(a.final_stats);
+  const unsigned long long* stage = reinterpret_cast<const unsigned long long*>(
+      reinterpret_cast<const unsigned char*>(ms) + sizeof(Misc));
+  int na = 0, nf = 0;
+  int agg_j = 0;                 // owned rows of item na already merged
+  int dec_a = -1, dec_f = -1;    // items whose positions are decoded below
+  ItemPos ipa{}, ipf{};
+  SeqDesc sda{};
+  // staging buffer b holds the pairs of item nf or nf + 1 (the one with
+  // parity b): its item, whether it is collected directly, a copy in
+  // flight, all pairs in, the copy barrier's parity, source and chunks
+  int cp_item[2] = {-1, -1}, cp_nc[2] = {0, 0};
+  bool cp_direct[2] = {false, false}, cp_out[2] = {false, false}, cp_ready[2] = {false, false};
+  uint32_t cp_par[2] = {0, 0};
+  float cp_m[2] = {0.f, 0.f}, cp_z[2] = {0.f, 0.f};   // this lane's row, merged
+  const unsigned long long* cp_src[2] = {nullptr, nullptr};
+  const volatile int* pub_items = &ms->pub_items;
+  bool ok = true;
+  unsigned long long t_last = global_ns();
+  while (nf < n_my) {
+    bool prog = false;
+    // ---- owner step for item na
+    if (na < n_my && na <= nf + 2) {
+      if (dec_a != na) {
+        ipa = decode_item(a, blockIdx.x + na * G);
+        sda = a.seqs[ipa.s];
+        dec_a = na;
+      }
+      const int nc = sda.n_chunks, c = ipa.c;
+      const int n_own = (nc * a.wpad <= kStageSlots || c >= W) ? 0 : (W - 1 - c) / nc + 1;
+      if (agg_j >= n_own) {
+        ++na;
+        agg_j = 0;
+        prog = true;
+      } else {
+        const int g = lanes_per_row(nc);
+        const int j = agg_j + lane / g, sl = lane % g;
+        const int r = c + j * nc;
+        const bool act = j < n_own;
+        const unsigned long long* p0 =
+            part + ((int64_t)ipa.layer * a.items_per_layer + sda.item_base +
+                    (int64_t)ipa.h * nc) * a.wpad + (act ? r : 0);
+        const unsigned long long* pp[kPerLane];
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int ch = sl + k * g;
+          pp[k] = p0 + (int64_t)((act && ch < nc) ? ch : 0) * a.wpad;
+        }
+        unsigned long long v[kPerLane];
+        slot_read8(pp, v);
+        bool have = true;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k)
+          if (act && sl + k * g < nc) have &= v[k] != kEmptySlot;
+        if (__all_sync(0xffffffffu, have)) {
+          float m = -INFINITY, z = 0.f;
+#pragma unroll
+          for (int k = 0; k < kPerLane; ++k)
+            if (act && sl + k * g < nc)
+              merge_stats(m, z, __uint_as_float((uint32_t)v[k]),
+                          __uint_as_float((uint32_t)(v[k] >> 32)));
+          for (int off = g >> 1; off >= 1; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+            merge_stats(m, z, m2, z2);
+          }
+          if (act && sl == 0) {
+            if (m != m) m = INFINITY;
+            slot_publish(fslots + (int64_t)ipa.inst * a.wpad + r, m, z);
+          }
+          agg_j += 32 / g;
+          if (agg_j >= n_own) {
+            ++na;
+            agg_j = 0;
+          }
+          prog = true;
+        }
+      }
+    }
+    // ---- bulk copies for items nf and nf + 1, each issued once this
+    // CTA's own chunk of the item is published, repeated until every
+    // pair of the instance is in
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int x = (nf & 1) == b ? nf : nf + 1;
+      if (x >= n_my) continue;
+      if (cp_item[b] != x) {  // the buffer's previous item is collected
+        const ItemPos ipx = decode_item(a, blockIdx.x + x * G);
+        const SeqDesc sdx = a.seqs[ipx.s];
+        cp_item[b] = x;
+        cp_nc[b] = sdx.n_chunks;
+        cp_direct[b] = sdx.n_chunks * a.wpad <= kStageSlots;
+        cp_ready[b] = false;
+        cp_src[b] = part + ((int64_t)ipx.layer * a.items_per_layer + sdx.item_base +
+                            (int64_t)ipx.h * sdx.n_chunks) * a.wpad;
+      }
+      if (!cp_direct[b] || cp_ready[b]) continue;
+      const unsigned long long* buf_b = stage + b * kStageSlots;
+      if (!cp_out[b]) {
+        if (__shfl_sync(0xffffffffu, *pub_items > x ? 1 : 0, 0)) {
+          __syncwarp();  // every lane is done with the staging buffer
+          if (lane == 0) {
+            const uint32_t bytes = (uint32_t)(cp_nc[b] * a.wpad * 8);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(smem_u32(&ms->slot_bar[b]), bytes);
+            bulk_load(smem_u32(buf_b), cp_src[b], bytes, smem_u32(&ms->slot_bar[b]));
+          }
+          cp_out[b] = true;
+        }
+      } else if (__shfl_sync(0xffffffffu,
+                             mbar_try(smem_u32(&ms->slot_bar[b]), cp_par[b]) ? 1 : 0, 0)) {
+        mbar_wait(smem_u32(&ms->slot_bar[b]), cp_par[b], limit, nullptr);  // done: acquire
+        cp_par[b] ^= 1;
+        cp_out[b] = false;
+        // merge each row over the chunks in two passes (max, then the
+        // rescaled sum), checking that every pair is in; lane = row, and
+        // for W <= 16 a power of two, lane group q takes chunks q, q + ng,
+        // ... (the groups merged last)
+        const int ng = (W <= 16 && (W & (W - 1)) == 0) ? 32 / W : 1;
+        const int rpg = 32 / ng, r = lane % rpg, q = lane / rpg;
+        const int nc = cp_nc[b];
+        bool have = true;
+        float M = -INFINITY, Z = 0.f;
+        if (r < W) {
+          // four independent chains in each pass (a fixed order)
+          const unsigned long long* col = buf_b + r;
+          const int st = ng * a.wpad;
+          float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          int ch = q;
+          for (; ch + 3 * ng < nc; ch += 4 * ng) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const unsigned long long sv = col[(ch * a.wpad) + k * st];
+              have &= sv != kEmptySlot;
+              mk[k] = fmaxf(mk[k], __uint_as_float((uint32_t)sv));
+            }
+          }
+          for (; ch < nc; ch += ng) {
+            const unsigned long long sv = col[ch * a.wpad];
+            have &= sv != kEmptySlot;
+            mk[0] = fmaxf(mk[0], __uint_as_float((uint32_t)sv));
+          }
+          M = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
+          if (M != -INFINITY) {
+            float zk[4] = {0.f, 0.f, 0.f, 0.f};
+            ch = q;
+            for (; ch + 3 * ng < nc; ch += 4 * ng) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const unsigned long long sv = col[(ch * a.wpad) + k * st];
+                zk[k] = fmaf(__uint_as_float((uint32_t)(sv >> 32)),
+                             ex2(__uint_as_float((uint32_t)sv) - M), zk[k]);
+              }
+            }
+            for (; ch < nc; ch += ng) {
+              const unsigned long long sv = col[ch * a.wpad];
+              zk[0] = fmaf(__uint_as_float((uint32_t)(sv >> 32)),
+                           ex2(__uint_as_float((uint32_t)sv) - M), zk[0]);
+            }
+            Z = (zk[0] + zk[1]) + (zk[2] + zk[3]);
+          }
+        }
+        for (int off = 16; off >= rpg; off >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+          const float z2 = __shfl_xor_sync(0xffffffffu, Z, off);
+          merge_stats(M, Z, m2, z2);
+        }
+        cp_m[b] = M;
+        cp_z[b] = Z;
+        cp_ready[b] = __all_sync(0xffffffffu, have);
+        prog = true;
+      }
+    }
+    // ---- collection step for item nf
+    if (nf < na) {
+      const int fbuf = nf & 1;
+      const uint32_t fpar = (uint32_t)(nf >> 1) & 1;
+      const bool direct = fbuf ? cp_direct[1] : cp_direct[0];
+      const bool ready = fbuf ? cp_ready[1] : cp_ready[0];
+      float* fin = ms->fin[fbuf];
+      bool done = false;
+      if (direct) {
+        if (ready && __shfl_sync(0xffffffffu,
+                                 mbar_try(smem_u32(&ms->fempty[fbuf]), fpar ^ 1) ? 1 : 0, 0)) {
+          mbar_wait(smem_u32(&ms->fempty[fbuf]), fpar ^ 1, limit, nullptr);
+          const int ng = (W <= 16 && (W & (W - 1)) == 0) ? 32 / W : 1;
+          const int r = lane % (32 / ng);
+          const float M = fbuf ? cp_m[1] : cp_m[0], Z = fbuf ? cp_z[1] : cp_z[0];
+          if (lane < 32 / ng && r < W) fin[r] = M + log2f(Z);
+          if (fbuf) cp_ready[1] = false; else cp_ready[0] = false;
+          done = true;
+        }
+      } else if (__shfl_sync(0xffffffffu,
+                             mbar_try(smem_u32(&ms->fempty[fbuf]), fpar ^ 1) ? 1 : 0, 0)) {
+        if (dec_f != nf) {
+          ipf = decode_item(a, blockIdx.x + nf * G);
+          dec_f = nf;
+        }
+        const unsigned long long* f0 = fslots + (int64_t)ipf.inst * a.wpad;
+        unsigned long long f[2];
+        slot_read2(f0 + min(lane, W - 1), f0 + min(lane + 32, W - 1), f);
+        bool have = true;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (lane + 32 * k < W) have &= f[k] != kEmptySlot;
+        if (__all_sync(0xffffffffu, have)) {
+          mbar_wait(smem_u32(&ms->fempty[fbuf]), fpar ^ 1, limit, nullptr);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int r = lane + 32 * k;
+            if (r < W)
+              fin[r] = __uint_as_float((uint32_t)f[k]) +
+                       log2f(__uint_as_float((uint32_t)(f[k] >> 32)));
+          }
+          done = true;
+        }
+      }
+      if (done) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int r = lane + 32 * k;
+          if (r >= W && r < NW) fin[r] = INFINITY;
+        }
+        mbar_arrive(smem_u32(&ms->ffull[fbuf]));
+        ++nf;
+        prog = true;
+      }
+    }
+    const unsigned long long now = global_ns();
+    if (prog) {
+      t_last = now;
+    } else if (__any_sync(0xffffffffu, *abort_flag != 0 || now - t_last > limit)) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok && lane == 0) {
+    *abort_flag = 1;
+    record_status(a.status, KVSEL_ERR_TIMEOUT);
+  }
+  // a bulk copy still in flight must land before the CTA exits
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+    if (cp_out[b] && lane == 0) mbar_wait(smem_u32(&ms->slot_bar[b]), cp_par[b], limit, nullptr);
+}
+
 // ACC: add the votes to those already in `votes` (the second pass of a
 // window-row split).
 template <int NW, int KD, bool LOGITS, bool ACC>
@@ -412,264 +674,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
       }
     }
   } else if (warp == kStatsWarp) {
-    // ------------------------------------------------------------ statistics
-    // Collects, for each of this CTA's items in order, M_r + log2 Z_r of every
-    // row of its instance for pass 2. Where the pairs of all chunks of the
-    // instance fit the staging buffer, one bulk copy brings them into shared
-    // memory (repeated until every pair is published) and the warp merges
-    // each row over the chunks in chunk order. Larger instances go through
-    // owners: row r is merged by chunk r mod nc (same order), which publishes
-    // the instance's final pair of that row; every chunk then reads the W
-    // final pairs. The owner step runs ahead of the collection step; each
-    // turn of the loop issues its loads together.
-    if constexpr (!LOGITS) {
-      constexpr int kStageSlots = slot_stage_for(NW) / 16;   // per staging buffer
-      const unsigned long long* part = reinterpret_cast<const unsigned long long*>(a.part);
-      unsigned long long* fslots = reinterpret_cast<unsigned long long*>(a.final_stats);
-      const unsigned long long* stage = reinterpret_cast<const unsigned long long*>(
-          reinterpret_cast<const unsigned char*>(ms) + sizeof(Misc));
-      int na = 0, nf = 0;
-      int agg_j = 0;                 // owned rows of item na already merged
-      int dec_a = -1, dec_f = -1;    // items whose positions are decoded below
-      ItemPos ipa{}, ipf{};
-      SeqDesc sda{};
-      // staging buffer b holds the pairs of item nf or nf + 1 (the one with
-      // parity b): its item, whether it is collected directly, a copy in
-      // flight, all pairs in, the copy barrier's parity, source and chunks
-      int cp_item[2] = {-1, -1}, cp_nc[2] = {0, 0};
-      bool cp_direct[2] = {false, false}, cp_out[2] = {false, false}, cp_ready[2] = {false, false};
-      uint32_t cp_par[2] = {0, 0};
-      float cp_m[2] = {0.f, 0.f}, cp_z[2] = {0.f, 0.f};   // this lane's row, merged
-      const unsigned long long* cp_src[2] = {nullptr, nullptr};
-      const volatile int* pub_items = &ms->pub_items;
-      bool ok = true;
-      unsigned long long t_last = global_ns();
-      while (nf < n_my) {
-        bool prog = false;
-        // ---- owner step for item na
-        if (na < n_my && na <= nf + 2) {
-          if (dec_a != na) {
-            ipa = decode_item(a, blockIdx.x + na * G);
-            sda = a.seqs[ipa.s];
-            dec_a = na;
-          }
-          const int nc = sda.n_chunks, c = ipa.c;
-          const int n_own = (nc * a.wpad <= kStageSlots || c >= W) ? 0 : (W - 1 - c) / nc + 1;
-          if (agg_j >= n_own) {
-            ++na;
-            agg_j = 0;
-            prog = true;
-          } else {
-            const int g = lanes_per_row(nc);
-            const int j = agg_j + lane / g, sl = lane % g;
-            const int r = c + j * nc;
-            const bool act = j < n_own;
-            const unsigned long long* p0 =
-                part + ((int64_t)ipa.layer * a.items_per_layer + sda.item_base +
-                        (int64_t)ipa.h * nc) * a.wpad + (act ? r : 0);
-            const unsigned long long* pp[kPerLane];
-#pragma unroll
-            for (int k = 0; k < kPerLane; ++k) {
-              const int ch = sl + k * g;
-              pp[k] = p0 + (int64_t)((act && ch < nc) ? ch : 0) * a.wpad;
-            }
-            unsigned long long v[kPerLane];
-            slot_read8(pp, v);
-            bool have = true;
-#pragma unroll
-            for (int k = 0; k < kPerLane; ++k)
-              if (act && sl + k * g < nc) have &= v[k] != kEmptySlot;
-            if (__all_sync(0xffffffffu, have)) {
-              float m = -INFINITY, z = 0.f;
-#pragma unroll
-              for (int k = 0; k < kPerLane; ++k)
-                if (act && sl + k * g < nc)
-                  merge_stats(m, z, __uint_as_float((uint32_t)v[k]),
-                              __uint_as_float((uint32_t)(v[k] >> 32)));
-              for (int off = g >> 1; off >= 1; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
-                merge_stats(m, z, m2, z2);
-              }
-              if (act && sl == 0) {
-                if (m != m) m = INFINITY;
-                slot_publish(fslots + (int64_t)ipa.inst * a.wpad + r, m, z);
-              }
-              agg_j += 32 / g;
-              if (agg_j >= n_own) {
-                ++na;
-                agg_j = 0;
-              }
-              prog = true;
-            }
-          }
-        }
-        // ---- bulk copies for items nf and nf + 1, each issued once this
-        // CTA's own chunk of the item is published, repeated until every
-        // pair of the instance is in
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int x = (nf & 1) == b ? nf : nf + 1;
-          if (x >= n_my) continue;
-          if (cp_item[b] != x) {  // the buffer's previous item is collected
-            const ItemPos ipx = decode_item(a, blockIdx.x + x * G);
-            const SeqDesc sdx = a.seqs[ipx.s];
-            cp_item[b] = x;
-            cp_nc[b] = sdx.n_chunks;
-            cp_direct[b] = sdx.n_chunks * a.wpad <= kStageSlots;
-            cp_ready[b] = false;
-            cp_src[b] = part + ((int64_t)ipx.layer * a.items_per_layer + sdx.item_base +
-                                (int64_t)ipx.h * sdx.n_chunks) * a.wpad;
-          }
-          if (!cp_direct[b] || cp_ready[b]) continue;
-          const unsigned long long* buf_b = stage + b * kStageSlots;
-          if (!cp_out[b]) {
-            if (__shfl_sync(0xffffffffu, *pub_items > x ? 1 : 0, 0)) {
-              __syncwarp();  // every lane is done with the staging buffer
-              if (lane == 0) {
-                const uint32_t bytes = (uint32_t)(cp_nc[b] * a.wpad * 8);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_expect_tx(smem_u32(&ms->slot_bar[b]), bytes);
-                bulk_load(smem_u32(buf_b), cp_src[b], bytes, smem_u32(&ms->slot_bar[b]));
-              }
-              cp_out[b] = true;
-            }
-          } else if (__shfl_sync(0xffffffffu,
-                                 mbar_try(smem_u32(&ms->slot_bar[b]), cp_par[b]) ? 1 : 0, 0)) {
-            mbar_wait(smem_u32(&ms->slot_bar[b]), cp_par[b], limit, nullptr);  // done: acquire
-            cp_par[b] ^= 1;
-            cp_out[b] = false;
-            // merge each row over the chunks in two passes (max, then the
-            // rescaled sum), checking that every pair is in; lane = row, and
-            // for W <= 16 a power of two, lane group q takes chunks q, q + ng,
-            // ... (the groups merged last)
-            const int ng = (W <= 16 && (W & (W - 1)) == 0) ? 32 / W : 1;
-            const int rpg = 32 / ng, r = lane % rpg, q = lane / rpg;
-            const int nc = cp_nc[b];
-            bool have = true;
-            float M = -INFINITY, Z = 0.f;
-            if (r < W) {
-              // four independent chains in each pass (a fixed order)
-              const unsigned long long* col = buf_b + r;
-              const int st = ng * a.wpad;
-              float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-              int ch = q;
-              for (; ch + 3 * ng < nc; ch += 4 * ng) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const unsigned long long sv = col[(ch * a.wpad) + k * st];
-                  have &= sv != kEmptySlot;
-                  mk[k] = fmaxf(mk[k], __uint_as_float((uint32_t)sv));
-                }
-              }
-              for (; ch < nc; ch += ng) {
-                const unsigned long long sv = col[ch * a.wpad];
-                have &= sv != kEmptySlot;
-                mk[0] = fmaxf(mk[0], __uint_as_float((uint32_t)sv));
-              }
-              M = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
-              if (M != -INFINITY) {
-                float zk[4] = {0.f, 0.f, 0.f, 0.f};
-                ch = q;
-                for (; ch + 3 * ng < nc; ch += 4 * ng) {
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    const unsigned long long sv = col[(ch * a.wpad) + k * st];
-                    zk[k] = fmaf(__uint_as_float((uint32_t)(sv >> 32)),
-                                 ex2(__uint_as_float((uint32_t)sv) - M), zk[k]);
-                  }
-                }
-                for (; ch < nc; ch += ng) {
-                  const unsigned long long sv = col[ch * a.wpad];
-                  zk[0] = fmaf(__uint_as_float((uint32_t)(sv >> 32)),
-                               ex2(__uint_as_float((uint32_t)sv) - M), zk[0]);
-                }
-                Z = (zk[0] + zk[1]) + (zk[2] + zk[3]);
-              }
-            }
-            for (int off = 16; off >= rpg; off >>= 1) {
-              const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
-              const float z2 = __shfl_xor_sync(0xffffffffu, Z, off);
-              merge_stats(M, Z, m2, z2);
-            }
-            cp_m[b] = M;
-            cp_z[b] = Z;
-            cp_ready[b] = __all_sync(0xffffffffu, have);
-            prog = true;
-          }
-        }
-        // ---- collection step for item nf
-        if (nf < na) {
-          const int fbuf = nf & 1;
-          const uint32_t fpar = (uint32_t)(nf >> 1) & 1;
-          const bool direct = fbuf ? cp_direct[1] : cp_direct[0];
-          const bool ready = fbuf ? cp_ready[1] : cp_ready[0];
-          float* fin = ms->fin[fbuf];
-          bool done = false;
-          if (direct) {
-            if (ready && __shfl_sync(0xffffffffu,
-                                     mbar_try(smem_u32(&ms->fempty[fbuf]), fpar ^ 1) ? 1 : 0, 0)) {
-              mbar_wait(smem_u32(&ms->fempty[fbuf]), fpar ^ 1, limit, nullptr);
-              const int ng = (W <= 16 && (W & (W - 1)) == 0) ? 32 / W : 1;
-              const int r = lane % (32 / ng);
-              const float M = fbuf ? cp_m[1] : cp_m[0], Z = fbuf ? cp_z[1] : cp_z[0];
-              if (lane < 32 / ng && r < W) fin[r] = M + log2f(Z);
-              if (fbuf) cp_ready[1] = false; else cp_ready[0] = false;
-              done = true;
-            }
-          } else if (__shfl_sync(0xffffffffu,
-                                 mbar_try(smem_u32(&ms->fempty[fbuf]), fpar ^ 1) ? 1 : 0, 0)) {
-            if (dec_f != nf) {
-              ipf = decode_item(a, blockIdx.x + nf * G);
-              dec_f = nf;
-            }
-            const unsigned long long* f0 = fslots + (int64_t)ipf.inst * a.wpad;
-            unsigned long long f[2];
-            slot_read2(f0 + min(lane, W - 1), f0 + min(lane + 32, W - 1), f);
-            bool have = true;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              if (lane + 32 * k < W) have &= f[k] != kEmptySlot;
-            if (__all_sync(0xffffffffu, have)) {
-              mbar_wait(smem_u32(&ms->fempty[fbuf]), fpar ^ 1, limit, nullptr);
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int r = lane + 32 * k;
-                if (r < W)
-                  fin[r] = __uint_as_float((uint32_t)f[k]) +
-                           log2f(__uint_as_float((uint32_t)(f[k] >> 32)));
-              }
-              done = true;
-            }
-          }
-          if (done) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int r = lane + 32 * k;
-              if (r >= W && r < NW) fin[r] = INFINITY;
-            }
-            mbar_arrive(smem_u32(&ms->ffull[fbuf]));
-            ++nf;
-            prog = true;
-          }
-        }
-        const unsigned long long now = global_ns();
-        if (prog) {
-          t_last = now;
-        } else if (__any_sync(0xffffffffu, *abort_flag != 0 || now - t_last > limit)) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok && lane == 0) {
-        *abort_flag = 1;
-        record_status(a.status, KVSEL_ERR_TIMEOUT);
-      }
-      // a bulk copy still in flight must land before the CTA exits
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-        if (cp_out[b] && lane == 0) mbar_wait(smem_u32(&ms->slot_bar[b]), cp_par[b], limit, nullptr);
-    }
+    if constexpr (!LOGITS) stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - kEpiWarp0;         // 0..7
@@ -963,6 +968,421 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 }
 
 // ---------------------------------------------------------------------------
+// Two-pass variant for long instances
+// ---------------------------------------------------------------------------
+
+// An instance whose chunks fill much of the GPU's tensor memory cannot keep
+// its exponentials on chip until its statistics are merged without stalling
+// the stream of K. Here the chunks' exponentials are not kept: pass 1 of an
+// item computes its row statistics from the logits and frees its tensor
+// memory at once; pass 2 of the same item runs `lag` items later in the
+// same CTA, when the instance's statistics are merged, recomputes the
+// logits from the same K tiles (read a second time, now from L2: the lag is
+// a few items, tens of MiB over the GPU) and turns them into votes:
+//   vote_j = sum over rows of 2^(x_rj * log2(e)/sqrt(D) - M_r - log2 Z_r).
+// Per step the producer, the MMA issuer and the epilogue take pass 1 of item
+// `step` (TMEM buffer 0, query buffer 0) and then pass 2 of item
+// `step - lag` (buffer 1, query buffer 1). Pass 2 of an item waits only for
+// passes 1 of chunks that come at most two rounds later (n_chunks <= 2 x
+// CTAs), whose steps come no later than its own (lag >= 2), and each of
+// those waits for earlier steps only, so every wait ends in a correct
+// program; each wait is bounded anyway.
+template <int NW, int KD>
+__global__ void __maxnreg__(kRegs) tc_score_rc_kernel(const __grid_constant__ TcParams P) {
+  constexpr int kHalves = KD / 64;
+  constexpr int kStageBytes = kTileM * KD * 2;
+  constexpr int kQBytes = NW * KD * 2;
+  constexpr int kTiles = tiles_per_item(NW);
+  constexpr int NH = NW / 2;                   // pass-1 rows per epilogue warp
+  constexpr uint32_t kIdesc = instr_desc(NW, kTileM);
+  const ScoreArgs& a = P.a;
+  const int stages = P.stages;
+  const int W = a.W;
+  const int G = gridDim.x;
+  const int lag = a.two_pass;
+  const int n_my = P.n_items > (int)blockIdx.x ? (P.n_items - 1 - (int)blockIdx.x) / G + 1 : 0;
+  const int n_steps = n_my > 0 ? n_my + lag : 0;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sk = smem;
+  unsigned char* sq = sk + (size_t)stages * kStageBytes;
+  Misc* ms = reinterpret_cast<Misc*>(sq + 2 * kQBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long limit = a.wait_limit_ns;
+  volatile int* abort_flag = &ms->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&ms->full[s]), 1);
+      mbar_init(smem_u32(&ms->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ms->qfull[b]), 1);
+      mbar_init(smem_u32(&ms->qempty[b]), 1);
+      for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&ms->tile_ready[b][t]), 1);
+      mbar_init(smem_u32(&ms->tmem_empty[b]), kEpiWarps);
+      mbar_init(smem_u32(&ms->ffull[b]), 32);
+      mbar_init(smem_u32(&ms->fempty[b]), kEpiWarps * 32);
+      mbar_init(smem_u32(&ms->slot_bar[b]), 1);
+    }
+    mbar_init(smem_u32(&ms->mma_done), 1);
+    ms->abort_flag = 0;
+    ms->pub_items = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ms->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ms->tmem_base;
+
+  uint32_t armed = 0, armed_par = 0, q_armed = 0, q_par = 0;
+  bool mma_issued = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmk))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmq))
+                   : "memory");
+      // pass 1 leaves its K tiles in L2 for pass 2, which reads them last
+      const uint64_t pol_k1 = policy_evict_last();
+      const uint64_t pol_k2 = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      const int seqs_per_layer = (int)(a.q_rows / a.q_W);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int step = 0; ok && step < n_steps; ++step) {
+        for (int pass = 0; ok && pass < 2; ++pass) {
+          const int it = pass == 0 ? step : step - lag;
+          if (it < 0 || it >= n_my) continue;
+          const ItemPos ip = decode_item(a, blockIdx.x + it * G);
+          const SeqDesc sd = a.seqs[ip.s];
+          const int tok0 = ip.c * a.chunk_tokens;
+          const int ntiles = (min(a.chunk_tokens, sd.len - tok0) + kTileM - 1) / kTileM;
+          const uint32_t qp = (uint32_t)it & 1;   // each query buffer serves one pass
+          if (!mbar_wait(smem_u32(&ms->qempty[pass]), qp ^ 1, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(smem_u32(&ms->qfull[pass]), kQBytes);
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_4d(smem_u32(sq + pass * kQBytes + hf * NW * 128), &P.tmq,
+                        smem_u32(&ms->qfull[pass]), hf * 64, ip.h, a.q_row0,
+                        ip.layer * seqs_per_layer + sd.index, pol_q);
+          q_armed |= 1u << pass;
+          q_par = (q_par & ~(1u << pass)) | (qp << pass);
+          const int krow0 = (int)(ip.layer * a.T + sd.tok_off + tok0);
+          const uint64_t pol_k = pass == 0 ? pol_k1 : pol_k2;
+          for (int t = 0; t < ntiles; ++t) {
+            if (!mbar_wait(smem_u32(&ms->empty[stage]), phase ^ 1, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(smem_u32(&ms->full[stage]), kStageBytes);
+#pragma unroll
+            for (int hf = 0; hf < kHalves; ++hf)
+              tma_load_3d(smem_u32(sk + stage * kStageBytes + hf * kTileM * 128), &P.tmk,
+                          smem_u32(&ms->full[stage]), hf * 64, ip.h / a.kv_group,
+                          krow0 + t * kTileM, pol_k);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(a.status, KVSEL_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sk_addr = smem_u32(sk), sq_addr = smem_u32(sq);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int step = 0; ok && step < n_steps; ++step) {
+        for (int pass = 0; ok && pass < 2; ++pass) {
+          const int it = pass == 0 ? step : step - lag;
+          if (it < 0 || it >= n_my) continue;
+          const ItemPos ip = decode_item(a, blockIdx.x + it * G);
+          const SeqDesc sd = a.seqs[ip.s];
+          const int tok0 = ip.c * a.chunk_tokens;
+          const int ntiles = (min(a.chunk_tokens, sd.len - tok0) + kTileM - 1) / kTileM;
+          const uint32_t use = (uint32_t)it & 1;  // buffer `pass` serves one pass
+          if (!mbar_wait(smem_u32(&ms->tmem_empty[pass]), use ^ 1, limit, abort_flag) ||
+              !mbar_wait(smem_u32(&ms->qfull[pass]), use, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int t = 0; t < ntiles; ++t) {
+            if (!mbar_wait(smem_u32(&ms->full[stage]), phase, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(pass * kBufCols + t * NW);
+#pragma unroll
+            for (int kk = 0; kk < KD / 16; ++kk) {
+              const uint32_t a_addr =
+                  sk_addr + stage * kStageBytes + (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
+              const uint32_t b_addr =
+                  sq_addr + pass * kQBytes + (kk >> 2) * (NW * 128) + (kk & 3) * 32;
+              tc_mma(d_tmem, smem_desc(a_addr), smem_desc(b_addr), kIdesc, kk > 0 ? 1u : 0u);
+            }
+            mma_issued = true;
+            tc_commit(smem_u32(&ms->empty[stage]));
+            tc_commit(smem_u32(&ms->tile_ready[pass][t]));
+            if (++stage == stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (ok) tc_commit(smem_u32(&ms->qempty[pass]));
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(a.status, KVSEL_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == kStatsWarp) {
+    stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - kEpiWarp0;         // 0..7
+    const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+    const int sub = e >> 2;                 // pass 1: row half; pass 2: tile parity
+    const int row0 = sub * NH;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * quarter) << 16);
+    const float s2 = a.scale_log2;
+    bool ok = true;
+    // parity of the next phase of tile_ready[b][t] is bit 16 * b + t (a
+    // pass-2 warp waits only on the tiles of its parity, each use of them)
+    uint32_t tph = 0;
+    for (int step = 0; step < n_steps; ++step) {
+      for (int pass = 0; pass < 2; ++pass) {
+        const int it = pass == 0 ? step : step - lag;
+        if (it < 0 || it >= n_my) continue;
+        const int item = blockIdx.x + it * G;
+        const ItemPos ip = decode_item(a, item);
+        const SeqDesc sd = a.seqs[ip.s];
+        const int tok0 = ip.c * a.chunk_tokens;
+        const int ntiles = (min(a.chunk_tokens, sd.len - tok0) + kTileM - 1) / kTileM;
+        const int prefix = sd.len - W;
+        const int pb = it & 1;                     // statistics buffers of this item
+        const uint32_t buf_addr = lane_addr + (uint32_t)(pass * kBufCols);
+        if (pass == 0) {
+          // ---- pass 1: per-row softmax statistics of this warp's tokens, as
+          // in the one-pass kernel (a warp-wide reference per row that moves
+          // only when a logit exceeds it by more than 32), nothing stored.
+          float mref[NH], zsum[NH];
+#pragma unroll
+          for (int i = 0; i < NH; ++i) {
+            mref[i] = -INFINITY;
+            zsum[i] = 0.f;
+          }
+          float ymin = INFINITY;
+          bool bad = false, fresh = true;
+          for (int t = 0; t < ntiles; ++t) {
+            const uint32_t tbit = 1u << t;
+            if (ok)
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(smem_u32(&ms->tile_ready[0][t]), (tph & tbit) ? 1u : 0u,
+                                        limit, abort_flag));
+            tph ^= tbit;
+            if (!ok) continue;
+            tc_fence_after();
+            const uint32_t taddr = buf_addr + (uint32_t)(t * NW + row0);
+            const int tbase = tok0 + t * kTileM + 32 * quarter;
+            const int tok = tbase + lane;
+            if (tbase + 31 < prefix) {
+              float y[NH];
+              tmem_load_cols<NH>(taddr, y);
+              if (fresh) {
+#pragma unroll
+                for (int i = 0; i < NH; ++i) mref[i] = __shfl_sync(0xffffffffu, y[i] * s2, 0);
+                fresh = false;
+              }
+              bool need = false;
+#pragma unroll
+              for (int i = 0; i < NH; ++i) {
+                y[i] = fmaf(y[i], s2, -mref[i]);
+                need |= y[i] > 32.f;
+              }
+              if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int i = 0; i < NH; ++i) {
+                  if (__any_sync(0xffffffffu, y[i] > 32.f)) {
+                    const float xs = y[i] + mref[i];
+                    if (!finite_f(xs)) bad = true;
+                    const float mx = warp_max(xs);
+                    zsum[i] *= ex2(mref[i] - mx);
+                    mref[i] = mx;
+                    y[i] = xs - mx;
+                  }
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < NH; ++i) {
+                ymin = fminf(ymin, y[i]);
+                zsum[i] += ex2(y[i]);
+              }
+            } else {
+              const int lo = max(0, tok - prefix - row0);
+              const int hi = tok < sd.len ? min(NH, W - row0) : 0;
+#pragma unroll
+              for (int cb = 0; cb < NH; cb += 8) {
+                float xb[8];
+                tmem_load_cols<8>(taddr + cb, xb);
+                bool need = false;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const int i = cb + u;
+                  xb[u] *= s2;
+                  if (i < hi && !finite_f(xb[u])) bad = true;
+                  need |= i < hi && i >= lo && xb[u] > mref[i] + 32.f;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                  for (int u = 0; u < 8; ++u) {
+                    const int i = cb + u;
+                    const bool vis = i < hi && i >= lo;
+                    if (__any_sync(0xffffffffu, vis && xb[u] > mref[i] + 32.f)) {
+                      const float mx = warp_max(vis ? xb[u] : -INFINITY);
+                      if (mref[i] != -INFINITY) zsum[i] *= ex2(mref[i] - mx);
+                      mref[i] = mx;
+                    }
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const int i = cb + u;
+                  zsum[i] += (i < hi && i >= lo) ? ex2(xb[u] - mref[i]) : 0.f;
+                }
+              }
+            }
+          }
+          // the logits are read: the buffer goes back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ms->tmem_empty[0]));
+          // hand the chunk's statistics over (as in the one-pass kernel)
+#pragma unroll
+          for (int i = 0; i < NH; ++i)
+            if (row0 + i < W && zsum[i] != zsum[i]) bad = true;
+          if (ymin == -INFINITY) bad = true;
+          if (bad) record_status(a.status, KVSEL_ERR_NONFINITE);
+          reduce_sum<NH>(zsum, lane);
+          constexpr int kLanesPerRow = 32 / NH;
+          if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NH; ++i) ms->wm[pb][quarter][row0 + i] = mref[i];
+          }
+          if (lane % kLanesPerRow == 0) ms->wz[pb][quarter][row0 + lane / kLanesPerRow] = zsum[0];
+          epi_bar();
+          if (warp == kEpiWarp0) {
+            for (int r = lane; r < W; r += 32) {
+              float m = ms->wm[pb][0][r], z = ms->wz[pb][0][r];
+#pragma unroll
+              for (int q = 1; q < 4; ++q) merge_stats(m, z, ms->wm[pb][q][r], ms->wz[pb][q][r]);
+              if (m != m) m = INFINITY;
+              if (!(a.inject == 1 && item == 0))
+                slot_publish(reinterpret_cast<unsigned long long*>(a.part) +
+                                 (int64_t)item * a.wpad + r, m, z);
+            }
+            if (lane == 0) *reinterpret_cast<volatile int*>(&ms->pub_items) = it + 1;
+          }
+        } else {
+          // ---- pass 2: votes from the recomputed logits and the instance's
+          // merged statistics F_r = M_r + log2 Z_r (+inf for padded rows, so
+          // their terms vanish). This warp takes the tiles of parity `sub`,
+          // all rows.
+          const int64_t plane = ((int64_t)ip.layer * a.H + ip.h) * a.T + sd.tok_off;
+          if (ok)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&ms->ffull[pb]), (uint32_t)(it >> 1) & 1, limit,
+                                      abort_flag));
+          const float* F = ms->fin[pb];
+          for (int t = sub; t < ntiles; t += 2) {
+            const uint32_t tbit = 1u << (16 + t);
+            if (ok)
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(smem_u32(&ms->tile_ready[1][t]), (tph & tbit) ? 1u : 0u,
+                                        limit, abort_flag));
+            tph ^= tbit;
+            if (!ok) continue;
+            tc_fence_after();
+            const int tok = tok0 + t * kTileM + 32 * quarter + lane;
+            float x[NW];
+            tmem_load_row<NW>(buf_addr + (uint32_t)(t * NW), x);
+            float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < NW; i += 4) {
+              const float4 f4 = *reinterpret_cast<const float4*>(F + i);
+              p[0] += ex2(fmaf(x[i], s2, -f4.x));
+              p[1] += ex2(fmaf(x[i + 1], s2, -f4.y));
+              p[2] += ex2(fmaf(x[i + 2], s2, -f4.z));
+              p[3] += ex2(fmaf(x[i + 3], s2, -f4.w));
+            }
+            if (tok < sd.len)
+              a.votes[plane + tok] = tok < prefix ? (p[0] + p[1]) + (p[2] + p[3]) : 0.f;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ms->tmem_empty[1]));
+          mbar_arrive(smem_u32(&ms->fempty[pb]));
+        }
+        if (!ok) *abort_flag = 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (ms->abort_flag) {
+    if (warp == 0 && lane == 0) {
+      for (int s = 0; s < kMaxStages; ++s)
+        if (armed & (1u << s))
+          mbar_wait(smem_u32(&ms->full[s]), (armed_par >> s) & 1, limit, nullptr);
+      for (int b = 0; b < 2; ++b)
+        if (q_armed & (1u << b))
+          mbar_wait(smem_u32(&ms->qfull[b]), (q_par >> b) & 1, limit, nullptr);
+    }
+    if (warp == kMmaWarp && lane == 0 && mma_issued) {
+      tc_commit(smem_u32(&ms->mma_done));
+      mbar_wait(smem_u32(&ms->mma_done), 0, limit, nullptr);
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -996,7 +1416,7 @@ bool make_qmap(CUtensorMap* m, const void* base, int D, int H, int W, int64_t se
   return r == CUDA_SUCCESS;
 }
 
-template <int NW, int KD, bool LOGITS, bool ACC>
+template <int NW, int KD, bool LOGITS, bool ACC, bool RC = false>
 cudaError_t launch_t(const ScoreArgs& a, int grid) {
   constexpr int kStageBytes = kTileM * KD * 2;
   constexpr int kQBytes = NW * KD * 2;
@@ -1013,7 +1433,7 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   p.a = a;
   p.stages = stages;
   p.n_items = a.layers * a.items_per_layer;
-  auto kern = tc_score_kernel<NW, KD, LOGITS, ACC>;
+  void (*kern)(const TcParams) = RC ? tc_score_rc_kernel<NW, KD> : tc_score_kernel<NW, KD, LOGITS, ACC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1032,6 +1452,19 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
 template <bool LOGITS>
 cudaError_t launch_mode(const ScoreArgs& a, int grid) {
   const int nw = tc_window_pad(a.W);
+  if (a.two_pass) {  // long instances: statistics and votes in two passes, never logits
+    if (LOGITS || a.accumulate || a.two_pass < 2) return cudaErrorInvalidValue;
+    if (a.D == 128) {
+      if (nw == 16) return launch_t<16, 128, false, false, true>(a, grid);
+      if (nw == 32) return launch_t<32, 128, false, false, true>(a, grid);
+      if (nw == 64) return launch_t<64, 128, false, false, true>(a, grid);
+    } else if (a.D == 64) {
+      if (nw == 16) return launch_t<16, 64, false, false, true>(a, grid);
+      if (nw == 32) return launch_t<32, 64, false, false, true>(a, grid);
+      if (nw == 64) return launch_t<64, 64, false, false, true>(a, grid);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.accumulate) {  // second pass of a split: at most 32 rows, never logits
     if (LOGITS) return cudaErrorInvalidValue;
     if (a.D == 128) {

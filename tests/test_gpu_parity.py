@@ -56,9 +56,13 @@ SCORE_CASES = [
     ("gen_f32_d64", 1, 4, 64, 32, "f32", "avg", 7, [1024, 33]),
     ("gen_bf16_d96", 1, 2, 96, 8, "bf16", "avg", 3, [600, 8]),
     ("gen_w80_d128", 1, 2, 128, 80, "bf16", "avg", 5, [900]),
-    # long prompts at 32 < W <= 64: the window rows are scored in two passes
-    ("tc_w64_split", 1, 2, 128, 64, "bf16", "avg", 7, [40000, 64, 1500]),
-    ("tc_w40_split", 1, 2, 64, 40, "bf16", "max", 5, [33500, 40]),
+    # long prompts (more than 64 work items per instance): the two-pass kernel,
+    # statistics first, then votes from recomputed logits
+    ("tc2_w64_d128", 1, 2, 128, 64, "bf16", "avg", 7, [40000, 64, 1500]),
+    ("tc2_w40_d64", 1, 2, 64, 40, "bf16", "max", 5, [33500, 40]),
+    ("tc2_w32_d128", 2, 2, 128, 32, "bf16", "avg", 7, [70000, 5000, 32, 66000]),
+    ("tc2_w16_d64", 1, 3, 64, 16, "bf16", "max", 3, [140000, 16]),
+    ("tc2_w5_d128", 1, 2, 128, 5, "bf16", "avg", 1, [139000, 2049]),
 ]
 
 
@@ -113,7 +117,9 @@ def test_score_path_choice():
     assert a.kvsel_score_path(sh, 32, 0) == 1
     assert a.kvsel_score_path(sh, 64, 1024) == 1
     assert a.kvsel_score_path(sh, 65, 1024) == 0
-    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 40000]), 64, 1024) == 2
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 40000]), 64, 1024) == 3
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 70000]), 32, 1024) == 3
+    assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 65536]), 32, 1024) == 1
     assert a.kvsel_score_path(a.Shape(1, 4, 128, a.KVSEL_BF16, [0, 32768]), 64, 1024) == 1
     assert a.kvsel_score_path(a.Shape(1, 4, 64, a.KVSEL_F32, [0, 5000]), 32, 0) == 0
     assert a.kvsel_score_path(a.Shape(1, 4, 96, a.KVSEL_BF16, [0, 5000]), 32, 0) == 0
