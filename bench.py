@@ -12,7 +12,10 @@ far larger than L2, so no flush is needed between steps.
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own copy of
 the workload (weak scaling, no collective on the data path); the timed region
-is bracketed by barriers and the slowest rank's time is reported.
+is bracketed by barriers and the slowest rank's time is reported. At one GPU
+the other named long-prompt workloads (cfg3: L = 131072, W = 64; cfg4: eight
+ragged sequences; cfg5: c = 0.9) are then timed the same way, each outside
+the headline's timed region, under the key "configs".
 """
 
 from __future__ import annotations
@@ -53,6 +56,8 @@ def parse_args():
     p.add_argument("--no-reverse", action="store_true",
                    help="skip the reverse-mask attention measurement")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip timing the other named workloads after the headline")
     p.add_argument("--cpu-steps", type=int, default=40)
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (small profiling cases)")
@@ -133,10 +138,33 @@ class OraclePool:
 
 
 def n_workers() -> int:
+    """Every host core this process may run on (one oracle process per core)."""
     try:
-        return max(1, min(16, len(os.sched_getaffinity(0))))
+        return max(1, len(os.sched_getaffinity(0)))
     except AttributeError:
-        return max(1, min(16, os.cpu_count() or 1))
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_fields(pool) -> dict:
+    return {"cores": pool.workers, "host_cores": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -157,7 +185,7 @@ def run_reference(args, rank, world):
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": describe(wl),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, **cpu_fields(pool), "kind": "oracle",
                          "sample": pool.sample_text()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -397,6 +425,76 @@ def measure_reverse(api, dev, iters=10):
     return res
 
 
+SCORE_KERNELS = {
+    1: "tc_score_kernel (window logits, softmax statistics, votes)",
+    2: "tc_score_kernel, two 32-row passes (algorithmic bytes count K once)",
+    3: "tc_score_rc_kernel (statistics, then votes from logits recomputed from K in L2)",
+}
+
+
+def score_bytes_of(wl) -> int:
+    """Algorithmic bytes of the scoring stage: K and the window queries of
+    every scored (layer, sequence, head), read once."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    scored = [l for l in wl.seq_lens if l >= wl.capacity]
+    return wl.layers * wl.heads * sum((l + wl.window) * wl.dim * eb for l in scored)
+
+
+def measure_config(api, wk, name, dev, uuid, peak, steps=50, warmup=5):
+    """One named workload timed like the headline step (fused kvsel_snapkv on
+    device-resident inputs, CUDA events on the launching stream, clocks sampled
+    during the timed region), then its stage times from the library's events."""
+    import torch
+    wl = wk.make_workload(name)
+    q, k, v = wk.device_tensors(wl, dev)
+    shape = api.shape_of(k, wl.offsets)
+    t_out = api.kvsel_out_tokens(shape, wl.capacity)
+    out_idx = torch.empty((wl.layers, t_out, wl.heads), dtype=torch.int32, device=dev)
+    out_k = torch.empty((wl.layers, t_out, wl.heads, wl.dim), dtype=k.dtype, device=dev)
+    out_v = torch.empty_like(out_k)
+
+    def step():
+        api.kvsel_snapkv(q, k, v, wl.offsets, wl.window, wl.capacity, wl.pool_kind, wl.pool_k,
+                         out_idx, out_k, out_v)
+
+    sampler = ClockSampler(uuid)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    api.kvsel_profile_begin(steps)
+    for _ in range(steps):
+        step()
+    stage_ms, calls = api.kvsel_profile_end()
+    clocks = sampler.stop()
+    st = api.kvsel_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after {name}: {api.kvsel_status_string(st)}")
+    score_ms = stage_ms[0] / calls
+    step_bytes = wl.roofline_bytes()
+    res = {"workload": f"{wl.name}: {wl.note}", "steps": steps, "warmup": warmup,
+           "ms_per_step": ms, "value": wl.head_tokens() / (ms * 1e-3), "unit": UNIT,
+           "score_kernel": SCORE_KERNELS.get(api.kvsel_score_path(shape, wl.window,
+                                                                   wl.capacity), "generic"),
+           "step_bytes": step_bytes,
+           "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / peak,
+           "score_bytes": score_bytes_of(wl),
+           "score_frac": score_bytes_of(wl) / (score_ms * 1e-3) / 1e9 / peak,
+           "stages_ms": {"score": score_ms, "select_gather": stage_ms[1] / calls,
+                         "calls": calls},
+           "clocks": clocks}
+    del q, k, v, out_idx, out_k, out_v
+    torch.cuda.empty_cache()
+    return res
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -484,9 +582,7 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status after timing: {api.kvsel_status_string(st)}")
 
-    eb = 2 if wl.dtype == "bf16" else 4
-    scored = [l for l in wl.seq_lens if l >= wl.capacity]
-    score_bytes = wl.layers * wl.heads * sum((l + wl.window) * wl.dim * eb for l in scored)
+    score_bytes = score_bytes_of(wl)
     score_ms = stage_ms[0] / calls
     peak, peak_kind = measured_peak_gbs()
     achieved = score_bytes / (score_ms * 1e-3) / 1e9
@@ -554,13 +650,24 @@ def main():
         times = [cpu_pool.step() for _ in range(args.cpu_steps)]
         cpu_pool.close()
         cpu_val = cpu_pool.workers * cpu_pool.tokens * len(times) / sum(times)
-        cpu = {"value": cpu_val, "unit": UNIT, "cores": cpu_pool.workers, "kind": "oracle",
+        cpu = {"value": cpu_val, "unit": UNIT, **cpu_fields(cpu_pool), "kind": "oracle",
                "sample": cpu_pool.sample_text()}
+
+    # The other long-prompt workloads, each timed like the headline step
+    # (outside the headline's timed region; one GPU only).
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        del q, k, v, out_k, out_v
+        torch.cuda.empty_cache()
+        configs = {}
+        for name in ("cfg2", "cfg3", "cfg4", "cfg5"):
+            if name != args.config:
+                configs[name] = measure_config(api, wk, name, dev, uuid, peak)
 
     if rank == 0:
         # score kernel(s) + select/gather: one tensor-core pass, two (row split),
         # or the CUDA-core statistics, merge and votes kernels
-        launches_per_step = {1: 2, 2: 3}.get(path, 4)
+        launches_per_step = {1: 2, 2: 3, 3: 2}.get(path, 4)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -569,11 +676,8 @@ def main():
             "config": describe(wl),
             "gbs": step_bytes / (ms * 1e-3) / 1e9 * world,
             "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / peak,
-            "roofline": {"bound": "hbm", "kernel": {1: "tc_score_kernel (window logits, softmax "
-                                                    "statistics, votes)",
-                                                 2: "tc_score_kernel, two 32-row passes "
-                                                    "(algorithmic bytes count K once)"}.get(
-                                                        path, "generic scoring kernels"),
+            "roofline": {"bound": "hbm", "kernel": SCORE_KERNELS.get(path,
+                                                                     "generic scoring kernels"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": score_traffic(wl.layers) if path == 1 and
@@ -587,6 +691,7 @@ def main():
             "decode": decode,
             "jacap": jacap,
             "reverse": reverse,
+            "configs": configs,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

@@ -22,6 +22,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvsel.so")
+# debug library: the same sources with -DKVSEL_DEBUG (bounds checks on every
+# gather and output write, BAD_INDEX instead of an out-of-range access)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libkvsel_debug.so")
 SOURCES = ["api.cu", "score_tc.cu", "score_generic.cu", "select.cu", "compact.cu",
            "decode.cu", "jacap.cu", "reverse.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,9 +38,10 @@ def nvcc() -> str:
     return cand
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+           *(["-DKVSEL_DEBUG"] if debug else []),
            "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
@@ -48,23 +53,26 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile every source and link libkvsel.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile every source and link libkvsel.so (debug: libkvsel_debug.so with
+    the bounds checks); returns the library path."""
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(BUILD_DEBUG if debug else BUILD, exist_ok=True)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "kvsel.h")]
-    if (not force and os.path.exists(LIB) and
-            os.path.getmtime(LIB) >= max(os.path.getmtime(d) for d in deps)):
-        return LIB
+    if (not force and os.path.exists(lib) and
+            os.path.getmtime(lib) >= max(os.path.getmtime(d) for d in deps)):
+        return lib
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="--verbose" in sys.argv, force="--force" in sys.argv))
+    print(build(verbose="--verbose" in sys.argv, force="--force" in sys.argv,
+                debug="--debug" in sys.argv))

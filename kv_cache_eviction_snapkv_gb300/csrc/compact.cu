@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(CompactArgs a) {
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const uint32_t e = e0 + u * step;
-        if (ok[u]) {
+        if (ok[u] && KVSEL_IN_BOUNDS(out_row0 + e / vpr < (layer + 1) * a.T_out * a.H,
+                                              a.status)) {
           const int64_t dst = (int64_t)e * VW;
           __stcs(reinterpret_cast<V*>(okb + dst), kv[u]);
           __stcs(reinterpret_cast<V*>(ovb + dst), vv[u]);

@@ -60,6 +60,11 @@ __device__ __forceinline__ const DecSeq& find_seq(const DecodeArgs& a, int rem) 
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const DecodeArgs& a, const T* cache, const T* app,
                                            int layer, const DecSeq& sq, int kvh, int j) {
+  // debug builds: row j of the instance lies in its cache rows or its g
+  // appended rows (else the cache's first row of the layer is read instead)
+  if (!KVSEL_IN_BOUNDS(j >= 0 && j < sq.n_rows + a.g && sq.row_off + sq.n_rows <= a.T &&
+                           kvh < a.Hkv, a.status))
+    return cache + (int64_t)layer * a.T * a.Hkv * a.D;
   if (j < sq.n_rows)
     return cache + (((int64_t)layer * a.T + sq.row_off + j) * a.Hkv + kvh) * a.D;
   const int64_t r = (int64_t)layer * a.S * a.g + (int64_t)sq.index * a.g + (j - sq.n_rows);
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     }
     const float v = acc * inv;
     bad |= !finite_f(v);
-    a.out[(int64_t)inst * a.D + d] = v;
+    if (KVSEL_IN_BOUNDS(inst < a.layers * a.S * a.H, a.status)) a.out[(int64_t)inst * a.D + d] = v;
   }
   if (threadIdx.x == 0 && a.lse) a.lse[inst] = (mx + log2f(sum)) * 0.6931471805599453f;
   if (bad) record_status(a.status, KVSEL_ERR_NONFINITE);

@@ -1027,7 +1027,8 @@ jacap_leverage_kernel(const __grid_constant__ LevParams Lp) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ms->tfree[b]));
-        if (t < P) a.scores[plane + t] = w * ss;
+        if (t < P && KVSEL_IN_BOUNDS(plane + t < (int64_t)a.layers * a.H * a.T, a.status))
+          a.scores[plane + t] = w * ss;
       }
     }
     if (!ok) {

@@ -34,6 +34,20 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t i, int dtyp
 
 __device__ __forceinline__ bool finite_f(float x) { return fabsf(x) <= 3.402823466e38f; }
 
+// Debug builds (-DKVSEL_DEBUG) check the index arithmetic of the gathers and
+// output writes against the bounds the host passed: a failed check records
+// KVSEL_ERR_BAD_INDEX and the access is skipped. Release builds compile the
+// checks away (the condition is not evaluated).
+__device__ __forceinline__ bool debug_in_bounds(bool ok, int* status) {
+  if (!ok) record_status(status, KVSEL_ERR_BAD_INDEX);
+  return ok;
+}
+#ifdef KVSEL_DEBUG
+#define KVSEL_IN_BOUNDS(cond, status) (::kvsel::debug_in_bounds((cond), (status)))
+#else
+#define KVSEL_IN_BOUNDS(cond, status) true
+#endif
+
 // Largest s in [0, n) with base_of(s) <= key (arrays sorted by base, base_of(0) <= key).
 template <typename F>
 __device__ __forceinline__ int upper_find(int n, int key, F base_of) {

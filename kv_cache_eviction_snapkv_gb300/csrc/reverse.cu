@@ -240,7 +240,8 @@ reverse_kernel(const __grid_constant__ RevParams R) {
     const int r = quarter * 32 + lane, i = i0 + r;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const float c2 = 1.4426950408889634f / sqrtf((float)kRD);
-    const bool row_ok = i < n;
+    // debug builds also check the row against the layer's rows
+    const bool row_ok = i < n && KVSEL_IN_BOUNDS(sq.tok_off + i < a.T, a.status);
     const int pos_i = kPos ? __ldg(a.pos + sq.tok_off + min(i, n - 1)) : i;
     auto allowed = [&](int j) -> bool {      // branch-free: j in the sequence and later than i
       if (kPos) return row_ok & (j < n) & (__ldg(a.pos + sq.tok_off + min(j, n - 1)) > pos_i);

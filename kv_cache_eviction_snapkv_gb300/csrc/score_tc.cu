@@ -245,12 +245,14 @@ __device__ __forceinline__ void rescale_row(uint32_t base, int col, int t, float
 // pair is published) and the warp merges each row over the chunks in chunk
 // order. Larger instances go through owners: row r is merged by chunk r mod nc
 // (same order), which publishes the instance's final pair of that row; every
-// chunk then reads the W final pairs. The owner step runs ahead of the
-// collection step; each turn of the loop issues its loads together.
+// chunk then reads the W final pairs. The owner step runs at most
+// `owner_ahead` items ahead of the collection step (the vote pass lags the
+// statistics pass by that much less two); each turn of the loop issues its
+// loads together.
 template <int NW>
 __device__ __forceinline__ void stats_warp_loop(const ScoreArgs& a, Misc* ms, int n_my, int G,
                                                 int lane, unsigned long long limit,
-                                                volatile int* abort_flag) {
+                                                volatile int* abort_flag, int owner_ahead) {
   const int W = a.W;
   constexpr int kStageSlots = slot_stage_for(NW) / 16;   // per staging buffer
   const unsigned long long* part = reinterpret_cast<const unsigned long long*>(a.part);
@@ -276,7 +278,7 @@ __device__ __forceinline__ void stats_warp_loop(const ScoreArgs& a, Misc* ms, in
   while (nf < n_my) {
     bool prog = false;
     // ---- owner step for item na
-    if (na < n_my && na <= nf + 2) {
+    if (na < n_my && na <= nf + owner_ahead) {
       if (dec_a != na) {
         ipa = decode_item(a, blockIdx.x + na * G);
         sda = a.seqs[ipa.s];
@@ -674,7 +676,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
       }
     }
   } else if (warp == kStatsWarp) {
-    if constexpr (!LOGITS) stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag);
+    if constexpr (!LOGITS) stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag, 2);
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - kEpiWarp0;         // 0..7
@@ -1166,7 +1168,9 @@ __global__ void __maxnreg__(kRegs) tc_score_rc_kernel(const __grid_constant__ Tc
       }
     }
   } else if (warp == kStatsWarp) {
-    stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag);
+    // the owners keep up with pass 1, which runs `lag` items ahead of the
+    // collection for pass 2
+    stats_warp_loop<NW>(a, ms, n_my, G, lane, limit, abort_flag, 2 + lag);
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - kEpiWarp0;         // 0..7

@@ -301,11 +301,19 @@ template <> struct CopyVec<8> { using T = uint2; };
 template <> struct CopyVec<4> { using T = uint32_t; };
 template <> struct CopyVec<2> { using T = uint16_t; };
 
+// Bounds of one instance's gather (checked in debug builds): source
+// positions in [0, src_len) of its sequence, output rows before dst_end.
+struct GatherBounds {
+  int src_len;
+  int64_t dst_end;
+};
+
 // Copies the instance's kept K and V rows (slot s <- position idx(s)) into
 // out_K / out_V with VW-byte vectors, several rows in flight per thread.
 template <int VW, typename IdxOf>
 __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int64_t src_tok0,
-                                            int64_t dst_row0, int h, IdxOf idx_of) {
+                                            int64_t dst_row0, int h, GatherBounds gb,
+                                            IdxOf idx_of) {
   using V = typename CopyVec<VW>::T;
   constexpr int kU = 4;
   const int vpr = (int)(a.row_bytes / VW);
@@ -314,23 +322,31 @@ __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int
   const char* vb = reinterpret_cast<const char*>(a.v);
   char* okb = reinterpret_cast<char*>(a.out_k);
   char* ovb = reinterpret_cast<char*>(a.out_v);
+  (void)gb;
   for (int e0 = threadIdx.x; e0 < total; e0 += kSelThreads * kU) {
     V kv[kU], vv[kU];
+    bool go[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int e = e0 + u * kSelThreads;
+      go[u] = false;
       if (e < total) {
         const int s = e / vpr, vi = e - s * vpr;
-        const int64_t src =
-            ((src_tok0 + idx_of(s)) * a.kv_H + h / a.kv_div) * a.row_bytes + (int64_t)vi * VW;
-        kv[u] = __ldcs(reinterpret_cast<const V*>(kb + src));
-        vv[u] = __ldcs(reinterpret_cast<const V*>(vb + src));
+        const int j = idx_of(s);
+        go[u] = KVSEL_IN_BOUNDS(j >= 0 && j < gb.src_len && dst_row0 + s < gb.dst_end,
+                                a.status);
+        if (go[u]) {
+          const int64_t src =
+              ((src_tok0 + j) * a.kv_H + h / a.kv_div) * a.row_bytes + (int64_t)vi * VW;
+          kv[u] = __ldcs(reinterpret_cast<const V*>(kb + src));
+          vv[u] = __ldcs(reinterpret_cast<const V*>(vb + src));
+        }
       }
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int e = e0 + u * kSelThreads;
-      if (e < total) {
+      if (go[u]) {
         const int s = e / vpr, vi = e - s * vpr;
         const int64_t dst = ((dst_row0 + s) * a.H + h) * a.row_bytes + (int64_t)vi * VW;
         __stcs(reinterpret_cast<V*>(okb + dst), kv[u]);
@@ -342,12 +358,13 @@ __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int
 
 template <typename IdxOf>
 __device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int64_t src_tok0,
-                                           int64_t dst_row0, int h, IdxOf idx_of) {
+                                           int64_t dst_row0, int h, GatherBounds gb,
+                                           IdxOf idx_of) {
   switch (a.vec_bytes) {
-    case 16: gather_rows<16>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
-    case 8: gather_rows<8>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
-    case 4: gather_rows<4>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
-    default: gather_rows<2>(a, n_rows, src_tok0, dst_row0, h, idx_of); break;
+    case 16: gather_rows<16>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    case 8: gather_rows<8>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    case 4: gather_rows<4>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    default: gather_rows<2>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
   }
 }
 
@@ -626,7 +643,8 @@ __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs
   }
   __syncthreads();
   cluster_sync();
-  gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, [&](int s) { return (int)idx[s]; });
+  gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, GatherBounds{P + a.W, out_row0 + a.C},
+             [&](int s) { return (int)idx[s]; });
 }
 
 // stage[c] = score of position jb + c (summed over `groups` planes T floats
@@ -725,7 +743,8 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     const int per = (L + cs - 1) / cs, s0 = min(L, (int)rank * per), s1 = min(L, s0 + per);
     for (int s = s0 + tid; s < s1; s += kSelThreads) out[(int64_t)s * a.H] = s;
     if (gather_here)
-      gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, [&](int s) { return s0 + s; });
+      gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, GatherBounds{L, out_row0 + L},
+                 [&](int s) { return s0 + s; });
     return;
   }
   const int P = L - a.W;
@@ -982,7 +1001,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   if (!gather_here) return;
   if (CS1) {
     const int kk = (int)k;
-    gather_any(a, a.C, src_tok0, out_row0, h, [&](int s) {
+    gather_any(a, a.C, src_tok0, out_row0, h, GatherBounds{L, out_row0 + a.C}, [&](int s) {
       return s < kk ? (int)(sortbuf[s] & 0xFFFFFFFFull) : P + (s - kk);
     });
   } else {

@@ -2,16 +2,25 @@
 kvsel_snapkv call over the whole workload).
 
 For every named workload:
-* sampled (layer, sequence, head) instances against the fp64 oracle: the kept
-  prefix set may differ only at positions whose oracle pooled score is within
-  1e-4 x (largest vote) of the (C - W)-th largest, the window follows in order,
-  and the GPU's score order agrees with the oracle's scores within that
-  tolerance;
+* 32 sampled (layer, sequence, head) instances, spread over layers, heads and
+  sequences, against the fp64 oracle: the kept prefix set may differ only at
+  positions whose oracle pooled score is within 1e-4 x (largest vote) of the
+  (C - W)-th largest, the window follows in order, and the GPU's score order
+  agrees with the oracle's scores within that tolerance;
 * every instance: kept prefix positions distinct and inside [0, P), the window
   P..L-1 last, bypass sequences kept whole, and out_K / out_V equal to K / V at
   the output indices (checked on the device with torch indexing).
+The small fp32 workload (4 heads, L = 1024, D = 64) is compared with the oracle
+element by element on every head: votes, pooled scores, indices and rows.
+The planted workload keeps every planted key the oracle keeps (and nearly all
+of them); the selection kernel, fed the oracle's pooled scores rounded to fp32,
+is bit-exact at the two long prefix lengths (131008 positions on an 8-CTA
+cluster, 65520 with exact ties at the budget boundary).
 Plus the all-equal-keys case at the c=0.9 workload's size, where every interior
 pooled score ties exactly and the smallest-index rule decides everything.
+
+The oracle's inputs for one instance are sliced from the seeded device tensors
+(the torch route of the input generator, bit-identical to its numpy route).
 """
 
 import numpy as np
@@ -24,6 +33,7 @@ from kv_cache_eviction_snapkv_gb300 import workloads as wk
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
+N_SAMPLES = 32
 
 
 def api():
@@ -39,6 +49,14 @@ def run_full(wl):
     st = api().kvsel_device_status()
     assert st == 0, api().kvsel_status_string(st)
     return q, k, v, out_idx, out_k, out_v
+
+
+def head_of(wl, q, k, v, layer, b, h):
+    """(q_win, K, V) of one instance in fp64, from the device tensors."""
+    o, length, W = wl.offsets[b], wl.seq_lens[b], wl.window
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    return (f(q[layer, b * W:(b + 1) * W, h]), f(k[layer, o:o + length, h]),
+            f(v[layer, o:o + length, h]))
 
 
 def check_all_instances(wl, k, v, out_idx, out_k, out_v):
@@ -68,38 +86,48 @@ def check_all_instances(wl, k, v, out_idx, out_k, out_v):
         oo += n
 
 
-def check_sampled(wl, out_idx, samples):
+def check_sampled(wl, tensors, out_idx, samples):
+    """Sampled instances against the oracle; returns {(layer, b, h): oracle result}."""
+    q, k, v = tensors
     W, C = wl.window, wl.capacity
     n_keep = C - W
     idx = out_idx.cpu().numpy()
     out_offs = np.concatenate([[0], np.cumsum([min(l, C) for l in wl.seq_lens])])
-    ties = []
+    refs = {}
     for layer, b, h in samples:
         length = wl.seq_lens[b]
-        if length < C:
-            continue
-        qh, kh, vh = wk.head_inputs(wl, layer, b, h)
-        ref = oracle.snapkv_head(qh, kh, vh, C, wl.pool_k, wl.pooling)
         oo = out_offs[b]
-        got = idx[layer, oo:oo + C, h].tolist()
+        qh, kh, vh = head_of(wl, q, k, v, layer, b, h)
+        ref = oracle.snapkv_head(qh, kh, vh, C, wl.pool_k, wl.pooling)
+        refs[layer, b, h] = ref
+        got = idx[layer, oo:oo + min(length, C), h].tolist()
+        if length < C:
+            assert got == ref["indices"]
+            continue
         assert got[n_keep:] == ref["indices"][n_keep:]
         tol = VOTE_RTOL * ref["votes"].max()
         ok, msg = kept_set_ok(got[:n_keep], ref, n_keep, tol)
         assert ok, f"layer {layer} seq {b} head {h}: {msg}"
         pooled = ref["pooled"][got[:n_keep]]
         assert np.all(pooled[1:] <= pooled[:-1] + tol), "kept positions out of score order"
-        kth = np.sort(ref["pooled"])[::-1][n_keep - 1]
-        ties.append(int(np.sum(ref["pooled"] == kth)))
-    return ties
+    return refs
 
 
-def _samples(wl, n, seed):
+def samples_of(wl, n, seed):
+    """n distinct (layer, sequence, head) instances spread over the workload:
+    every sequence and every head appear when n allows."""
     rng = np.random.default_rng(seed)
-    out = []
-    for _ in range(n):
-        b = int(rng.integers(0, wl.num_seqs))
-        out.append((int(rng.integers(0, wl.layers)), b, int(rng.integers(0, wl.heads))))
-    return out
+    total = wl.layers * wl.num_seqs * wl.heads
+    if total <= n:
+        return [(l, b, h) for l in range(wl.layers) for b in range(wl.num_seqs)
+                for h in range(wl.heads)]
+    out = set()
+    i = 0
+    while len(out) < n:   # round-robin over sequences and heads, random layers
+        b, h = i % wl.num_seqs, (i * 7 + i // wl.num_seqs) % wl.heads
+        out.add((int(rng.integers(0, wl.layers)), b, h))
+        i += 1
+    return sorted(out)
 
 
 @pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4", "cfg5"])
@@ -107,13 +135,84 @@ def test_full_size_workload(name):
     wl = wk.make_workload(name)
     q, k, v, out_idx, out_k, out_v = run_full(wl)
     check_all_instances(wl, k, v, out_idx, out_k, out_v)
-    samples = _samples(wl, 3, 7)
-    if name == "cfg4":   # include every sequence, the bypassed one too
-        samples = [(0, b, (3 * b) % wl.heads) for b in range(wl.num_seqs)]
-    ties = check_sampled(wl, out_idx, samples)
-    if name == "cfg5":
-        print("exact ties at the budget boundary (sampled heads):", ties)
+    samples = samples_of(wl, N_SAMPLES, 7)
+    assert len(samples) >= min(N_SAMPLES, wl.layers * wl.num_seqs * wl.heads)
+    refs = check_sampled(wl, (q, k, v), out_idx, samples)
+    if name == "cfg3":
+        # the planted keys: every one the oracle keeps is kept, and nearly all
+        # are kept (a planted logit is +6 above its draw, which can be low)
+        n_keep = wl.capacity - wl.window
+        idx = out_idx.cpu().numpy()
+        planted = kept_planted = 0
+        for h in range(wl.heads):
+            pos = wk._plant_rows(wl, 0, 0, h)[0]
+            kept = set(idx[0, :n_keep, h].tolist())
+            ref_kept = set(refs[0, 0, h]["indices"][:n_keep])
+            assert all(int(p) in kept for p in pos if int(p) in ref_kept), f"head {h}"
+            planted += len(pos)
+            kept_planted += sum(int(p) in kept for p in pos)
+        assert kept_planted >= 0.9 * planted, (kept_planted, planted)
     del q, k, v, out_idx, out_k, out_v
+    torch.cuda.empty_cache()
+
+
+def test_small_fp32_workload_every_head():
+    """The small fp32 workload (N(0,1) * 2/sqrt(D), seed 1001), every head
+    element by element: votes and pooled scores within 1e-4 x the head's
+    largest vote, the kept set up to near-ties at the cut, the window, and
+    the gathered rows."""
+    wl = wk.make_workload("cfg1")
+    q, k, v, out_idx, out_k, out_v = run_full(wl)
+    check_all_instances(wl, k, v, out_idx, out_k, out_v)
+    votes, pooled = api().kvsel_score(q, k, wl.offsets, wl.window, wl.pool_kind, wl.pool_k)
+    assert api().kvsel_device_status() == 0
+    vg, pg = votes.cpu().numpy(), pooled.cpu().numpy()
+    samples = [(0, 0, h) for h in range(wl.heads)]
+    refs = check_sampled(wl, (q, k, v), out_idx, samples)
+    P = wl.seq_lens[0] - wl.window
+    for (_, _, h), ref in refs.items():
+        tol = VOTE_RTOL * ref["votes"].max()
+        np.testing.assert_allclose(vg[0, h, :P], ref["votes"], atol=tol, rtol=0)
+        np.testing.assert_allclose(pg[0, h, :P], ref["pooled"], atol=tol, rtol=0)
+        assert np.all(vg[0, h, P:] == 0) and np.all(pg[0, h, P:] == 0)
+
+
+@pytest.mark.parametrize("name,heads", [("cfg3", [0, 1]), ("cfg5", [14, 16, 0])])
+def test_full_size_select_bitexact(name, heads):
+    """kvsel_select on the oracle's pooled scores rounded to fp32, at the long
+    prefix lengths (cfg3: 131008 positions on an 8-CTA cluster; cfg5: 65520
+    positions, C - W = 6538, exact ties at the budget boundary). The oracle
+    re-runs its selection on the same fp32 values; the GPU must match it
+    exactly. Heads not listed get all-zero scores (every position ties: the
+    first C - W positions are kept)."""
+    ensure_built()
+    wl = wk.make_workload(name)
+    q, k, v = wk.device_tensors(wl, DEV)
+    L, W, C = wl.seq_lens[0], wl.window, wl.capacity
+    n_keep = C - W
+    pooled = torch.zeros((1, wl.heads, L), dtype=torch.float32)
+    want = {}
+    straddles = 0
+    for h in heads:
+        qh, kh, vh = head_of(wl, q, k, v, 0, 0, h)
+        ref = oracle.snapkv_head(qh, kh, vh, C, wl.pool_k, wl.pooling)
+        p32 = ref["pooled"].astype(np.float32)
+        pooled[0, h, :L - W] = torch.from_numpy(p32)
+        want[h] = oracle.select_from_pooled(p32.astype(np.float64), L, W, C)
+        kth = np.sort(p32)[::-1][n_keep - 1]
+        if np.sum(p32 == kth) > 1 and np.sum(p32 >= kth) > n_keep:
+            straddles += 1          # equal scores on both sides of the cut
+    del q, k, v
+    out_idx = api().kvsel_select(pooled.to(DEV), wl.offsets, wl.heads, W, C)
+    assert api().kvsel_device_status() == 0
+    got = out_idx.cpu().numpy()
+    for h in range(wl.heads):
+        if h in want:
+            assert got[0, :, h].tolist() == list(want[h]), f"head {h}"
+        else:
+            assert got[0, :, h].tolist() == list(range(n_keep)) + list(range(L - W, L))
+    if name == "cfg5":
+        assert straddles > 0, "no sampled head has tied scores across the cut"
     torch.cuda.empty_cache()
 
 

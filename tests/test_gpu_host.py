@@ -1,16 +1,22 @@
-"""kvsel_snapkv_host (cache in host memory) against the device path.
+"""kvsel_snapkv_host (cache in host memory) against the device path and the
+oracle.
 
 The host path runs the same kernels one layer at a time on q_win and K copied
 to the device, with V and the outputs in pinned host memory; its outputs must
-be bit-identical to kvsel_snapkv's on the same inputs.
+be bit-identical to kvsel_snapkv's on the same inputs, and on a ragged case
+they are also checked against the fp64 oracle directly: kept prefix sets up
+to near-ties at the cut, the window in order, bypass rows whole, and the
+gathered rows equal to the host K and V at the output indices.
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
-from helpers import ensure_built
+import oracle
+from helpers import VOTE_RTOL, ensure_built, kept_set_ok
 from kv_cache_eviction_snapkv_gb300 import workloads as wk
 
 pytestmark = pytest.mark.gpu
@@ -83,3 +89,38 @@ def test_unpinned_v_or_output_is_rejected():
     assert lib.kvsel_snapkv_host(sh.ref, p(q), p(k), p(vd), 8, 32, 0, 3, p(oi), p(ok), p(ov),
                                  None) == a.KVSEL_ERR_INVALID_ARG
     assert_ok()
+
+
+def test_host_path_against_oracle():
+    a = api()
+    wl = wk.custom_workload("host_oracle", 2, 3, 128, 16, 200, "bf16", "avg", 5,
+                            [1500, 90, 2700, 200], 91)
+    qh, kh, vh = (wk.storage_to_torch(x, wl.dtype) for x in wk.host_tensors(wl))
+    qh, kh, vh = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+    stream = torch.cuda.Stream()
+    oi, ok_, ov = a.kvsel_snapkv_host(qh, kh, vh, wl.offsets, wl.window, wl.capacity,
+                                      wl.pool_kind, wl.pool_k, stream=stream)
+    stream.synchronize()
+    assert_ok()
+    n_keep = wl.capacity - wl.window
+    idx = oi.numpy()
+    oo = 0
+    for b, length in enumerate(wl.seq_lens):
+        n = min(length, wl.capacity)
+        o = wl.offsets[b]
+        for layer in range(wl.layers):
+            for h in range(wl.heads):
+                q, k, v = wk.head_inputs(wl, layer, b, h)
+                ref = oracle.snapkv_head(q, k, v, wl.capacity, wl.pool_k, wl.pooling)
+                got = idx[layer, oo:oo + n, h].tolist()
+                if length < wl.capacity:
+                    assert got == ref["indices"]
+                else:
+                    assert got[n_keep:] == ref["indices"][n_keep:]
+                    tol = VOTE_RTOL * ref["votes"].max()
+                    good, msg = kept_set_ok(got[:n_keep], ref, n_keep, tol)
+                    assert good, f"layer {layer} seq {b} head {h}: {msg}"
+                rows = torch.tensor([o + j for j in got])
+                assert torch.equal(ok_[layer, oo:oo + n, h], kh[layer, rows, h])
+                assert torch.equal(ov[layer, oo:oo + n, h], vh[layer, rows, h])
+        oo += n
