@@ -295,6 +295,14 @@ __device__ __forceinline__ float pool_any(const float* s, int c, int kind, int k
 
 constexpr int kMaxE = 32;  // slice positions per thread of one CTA
 
+// Variants that sort more than 8192 kept keys (R >= 16) need at least 139 KiB
+// of shared memory, so they run one CTA per SM: they take the registers of two
+// and keep twice as many gathered rows in flight.
+template <int R> constexpr int kSelCtasPerSm = R >= 16 ? 1 : 2;
+static_assert(kMaxE * kSelWarps <= kSelThreads && kMaxE * kSelWarps <= kBins,
+              "the straddling slice's (row, warp) counts fit one per thread in the histogram");
+template <int R> constexpr int kGatherU = R >= 16 ? 8 : 4;
+
 template <int VW> struct CopyVec;
 template <> struct CopyVec<16> { using T = uint4; };
 template <> struct CopyVec<8> { using T = uint2; };
@@ -310,12 +318,11 @@ struct GatherBounds {
 
 // Copies the instance's kept K and V rows (slot s <- position idx(s)) into
 // out_K / out_V with VW-byte vectors, several rows in flight per thread.
-template <int VW, typename IdxOf>
+template <int VW, int kU, typename IdxOf>
 __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int64_t src_tok0,
                                             int64_t dst_row0, int h, GatherBounds gb,
                                             IdxOf idx_of) {
   using V = typename CopyVec<VW>::T;
-  constexpr int kU = 4;
   const int vpr = (int)(a.row_bytes / VW);
   const int total = n_rows * vpr;
   const char* kb = reinterpret_cast<const char*>(a.k);
@@ -356,15 +363,17 @@ __device__ __forceinline__ void gather_rows(const SelectArgs& a, int n_rows, int
   }
 }
 
-template <typename IdxOf>
+// kU rows of K and of V in flight per thread (8 where the kernel runs one
+// CTA per SM and has the registers for it).
+template <int kU, typename IdxOf>
 __device__ __forceinline__ void gather_any(const SelectArgs& a, int n_rows, int64_t src_tok0,
                                            int64_t dst_row0, int h, GatherBounds gb,
                                            IdxOf idx_of) {
   switch (a.vec_bytes) {
-    case 16: gather_rows<16>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
-    case 8: gather_rows<8>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
-    case 4: gather_rows<4>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
-    default: gather_rows<2>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    case 16: gather_rows<16, kU>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    case 8: gather_rows<8, kU>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    case 4: gather_rows<4, kU>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
+    default: gather_rows<2, kU>(a, n_rows, src_tok0, dst_row0, h, gb, idx_of); break;
   }
 }
 
@@ -624,6 +633,7 @@ __device__ bool bucket_sort(unsigned long long* buf, unsigned long long* tmp, in
 // its shared window) into `idx` and writes them to out_idx (`out`, stride H),
 // waits at a cluster barrier (after which the leader's shared memory may go),
 // then copies the rows.
+template <int kU>
 __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs, uint32_t rank,
                                   uint32_t sort_r, int32_t* idx, int32_t* out, int64_t src_tok0,
                                   int64_t out_row0, int h) {
@@ -643,8 +653,8 @@ __device__ void select_copy_share(const SelectArgs& a, uint32_t k, int P, int cs
   }
   __syncthreads();
   cluster_sync();
-  gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, GatherBounds{P + a.W, out_row0 + a.C},
-             [&](int s) { return (int)idx[s]; });
+  gather_any<kU>(a, s1 - s0, src_tok0, out_row0 + s0, h, GatherBounds{P + a.W, out_row0 + a.C},
+                 [&](int s) { return (int)idx[s]; });
 }
 
 // stage[c] = score of position jb + c (summed over `groups` planes T floats
@@ -743,8 +753,8 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     const int per = (L + cs - 1) / cs, s0 = min(L, (int)rank * per), s1 = min(L, s0 + per);
     for (int s = s0 + tid; s < s1; s += kSelThreads) out[(int64_t)s * a.H] = s;
     if (gather_here)
-      gather_any(a, s1 - s0, src_tok0, out_row0 + s0, h, GatherBounds{L, out_row0 + L},
-                 [&](int s) { return s0 + s; });
+      gather_any<kGatherU<R>>(a, s1 - s0, src_tok0, out_row0 + s0, h,
+                              GatherBounds{L, out_row0 + L}, [&](int s) { return s0 + s; });
     return;
   }
   const int P = L - a.W;
@@ -919,31 +929,46 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   // ---- emit kept keys (composite ~key << 32 | position) into the leader.
   // Phase 1 marks kept keys (bit m of `mask` for slice index tid + m*NT) and
   // counts them per warp; phase 2 writes them at consecutive places.
-  uint32_t mask = 0, eq_seen = 0;
+  uint32_t mask = 0;
   if (all_eq || take_eq == 0) {
     for (int m = 0, i = tid; m < kMaxE && i < n; ++m, i += kSelThreads) {
       const uint32_t key = keys[i];
       if (key > thr || (all_eq && key == thr)) mask |= 1u << m;
     }
   } else {
-    // the straddling slice: rank equal keys in position order, row by row
-    for (int m = 0; m < kMaxE && m * kSelThreads < n; ++m) {
+    // the straddling slice: rank the equal keys in position order (row m,
+    // then warp, then lane): the equal keys of every (row, warp) counted by
+    // ballots, one block-wide exclusive scan over those counts in that
+    // order (at most kMaxE * kSelWarps = kSelThreads of them, one per
+    // thread, in the histogram's words, free here), then each key's rank
+    const int rows = min(kMaxE, (n + kSelThreads - 1) / kSelThreads);
+    uint32_t* eqc = sh.hist;
+    for (int m = 0; m < rows; ++m) {
+      const int i = tid + m * kSelThreads;
+      const uint32_t bal = __ballot_sync(0xffffffffu, i < n && keys[i] == thr);
+      if (lane == 0) eqc[m * kSelWarps + warp] = __popc(bal);
+    }
+    __syncthreads();
+    const uint32_t c = tid < rows * kSelWarps ? eqc[tid] : 0u;
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) sh.wsum[warp] = incl;
+    __syncthreads();
+    uint32_t before = incl - c;
+    for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+    if (tid < rows * kSelWarps) eqc[tid] = before;
+    __syncthreads();
+    for (int m = 0; m < rows; ++m) {
       const int i = tid + m * kSelThreads;
       const uint32_t key = i < n ? keys[i] : 0u;
       const bool eq = i < n && key == thr;
       const uint32_t bal = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) sh.warp_cnt[warp][1] = __popc(bal);
-      __syncthreads();
-      uint32_t before = eq_seen, row = 0;
-      for (int w = 0; w < kSelWarps; ++w) {
-        const uint32_t c = sh.warp_cnt[w][1];
-        if (w < warp) before += c;
-        row += c;
-      }
-      before += __popc(bal & ((1u << lane) - 1u));
-      if ((i < n && key > thr) || (eq && before < take_eq)) mask |= 1u << m;
-      eq_seen += row;
-      __syncthreads();
+      const uint32_t rank = eqc[m * kSelWarps + warp] + __popc(bal & ((1u << lane) - 1u));
+      if ((i < n && key > thr) || (eq && rank < take_eq)) mask |= 1u << m;
     }
   }
   const uint32_t mine = __popc(mask);
@@ -973,7 +998,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
     // the leader sorts; then every CTA copies a share of the kept rows, its
     // positions read from the leader's sorted keys
     cluster_sync();
-    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
+    select_copy_share<kGatherU<R>>(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
                       src_tok0, out_row0, h);
     return;
   }
@@ -1001,13 +1026,14 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
   if (!gather_here) return;
   if (CS1) {
     const int kk = (int)k;
-    gather_any(a, a.C, src_tok0, out_row0, h, GatherBounds{L, out_row0 + a.C}, [&](int s) {
+    gather_any<kGatherU<R>>(a, a.C, src_tok0, out_row0, h, GatherBounds{L, out_row0 + a.C},
+                            [&](int s) {
       return s < kk ? (int)(sortbuf[s] & 0xFFFFFFFFull) : P + (s - kk);
     });
   } else {
     __syncthreads();
     cluster_sync();
-    select_copy_share(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
+    select_copy_share<kGatherU<R>>(a, k, P, cs, rank, sort_r, reinterpret_cast<int32_t*>(smem), out,
                       src_tok0, out_row0, h);
   }
 }
@@ -1020,7 +1046,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
 // other copies. The wait is on a CTA that is already running and is bounded
 // (running out of time only costs speed).
 template <int R, bool CS1>
-__global__ void __launch_bounds__(kSelThreads, 2) select_kernel(const __grid_constant__ SelectArgs a) {
+__global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm<R>) select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ SelShared sh;
   int* selected = nullptr;
