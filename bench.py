@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--cpu-steps", type=int, default=40)
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (small profiling cases)")
+    p.add_argument("--heads", type=int, default=0,
+                   help="override the workload's head count (small profiling cases)")
     return p.parse_args()
 
 
@@ -427,7 +429,6 @@ def measure_reverse(api, dev, iters=10):
 
 SCORE_KERNELS = {
     1: "tc_score_kernel (window logits, softmax statistics, votes)",
-    2: "tc_score_kernel, two 32-row passes (algorithmic bytes count K once)",
     3: "tc_score_rc_kernel (statistics, then votes from logits recomputed from K in L2)",
 }
 
@@ -532,6 +533,8 @@ def main():
     wl = wk.make_workload(args.config)
     if args.layers:
         wl.layers = args.layers
+    if args.heads:
+        wl.heads = args.heads
     wl.seed = shard.rank_seed(wl.seed, rank)   # rank r's own batch (weak scaling)
     q, k, v = wk.device_tensors(wl, dev)
     shape = api.shape_of(k, wl.offsets)
@@ -667,7 +670,7 @@ def main():
     if rank == 0:
         # score kernel(s) + select/gather: one tensor-core pass, two (row split),
         # or the CUDA-core statistics, merge and votes kernels
-        launches_per_step = {1: 2, 2: 3, 3: 2}.get(path, 4)
+        launches_per_step = {1: 2, 3: 2}.get(path, 4)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

@@ -112,10 +112,11 @@ const char* kvsel_status_string(kvsel_status status);
 int64_t kvsel_out_tokens(const kvsel_shape* shape, int32_t C);
 
 /* Which window-logit kernel a call with this shape takes: 1 = the tensor-core
- * kernel (TMA + tcgen05, bf16, D in {64,128}, W <= 64), 2 = the tensor-core
- * kernel in two passes over the window rows (32 < W <= 64 on prompts longer
- * than 64 of its 512-token items; K is read twice), 0 = the CUDA-core kernel
- * (any other supported shape), -1 = the call would be rejected.
+ * kernel (TMA + tcgen05, bf16, D in {64,128}, W <= 64), 3 = the tensor-core
+ * two-pass kernel (the same shapes, on sequences longer than 64 of the
+ * kernel's work items: row statistics first, then the votes from logits
+ * recomputed from K, which the second pass reads from L2), 0 = the CUDA-core
+ * kernel (any other supported shape), -1 = the call would be rejected.
  * C = 0 means "score every sequence" (kvsel_score); otherwise sequences with
  * L < C are not scored. Host only; queries the current device. */
 int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C);

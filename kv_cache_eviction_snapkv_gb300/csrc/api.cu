@@ -227,10 +227,7 @@ struct ScorePass {
   std::vector<SeqDesc> scored;
   int items_per_layer = 0, inst_per_layer = 0, max_chunks = 0;
   int chunk = 0, wpad = 0;
-  int W = 0;           // window rows of this pass (its causal mask and statistics)
-  int q_row0 = 0;      // the first of them within each sequence's rows of q_win
-  int vote_cut = 0;    // votes kept for tok < L - W - vote_cut of the pass's L
-  int accumulate = 0;  // added to the votes of the previous pass
+  int W = 0;           // window rows (the causal mask and statistics)
   int two_pass = 0;    // > 0: the two-pass kernel with this lag (long instances)
 };
 
@@ -238,18 +235,6 @@ struct ScorePlan {
   bool tc = false;
   std::vector<ScorePass> passes;
 };
-
-// Window-row split (tensor cores, 32 < W <= 64, long prompts). A selection's
-// votes are a sum over window rows, and every row's softmax is its own, so
-// rows 0 .. 31 (queries P .. P+31, which see only the first P + 32 tokens)
-// and rows 32 .. W-1 can be scored as two instances of at most 32 rows, the
-// second adding its votes to the first's. Each pass keeps at most 32 columns
-// of exponentials per token on chip instead of 64, so the instances of a pass
-// take half the tensor memory and the chunks' statistics exchange overlaps the
-// streaming of K as at W <= 32; the price is reading K twice. (The second
-// pass's padded rows, beyond W, read as zeros, as in a single pass.) Used once
-// an instance exceeds kSplitChunks items of the 64-row kernel.
-constexpr int kSplitChunks = 64;
 
 // Long instances (more than kTwoPassChunks work items) take the two-pass
 // kernel: pass 1 of an item computes its row statistics and frees its tensor
@@ -265,11 +250,9 @@ constexpr int kTwoPassChunks = KVSEL_TWO_PASS_CHUNKS;
 constexpr int kTwoPassLag = KVSEL_TWO_PASS_LAG;
 
 kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* k,
-                        const DevState* d, ScorePlan* sp, bool allow_split = true) {
+                        const DevState* d, ScorePlan* sp, bool allow_two_pass = true) {
   const bool tc_ok = d->cc_major == 10 && tc_eligible(p.dtype, p.D, W, q, k);
-  // len_cut: tokens dropped from the end of every sequence (the last rows of
-  // the window that this pass leaves out)
-  auto build = [&](ScorePass& ps, int chunk, int wpad, int len_cut) {
+  auto build = [&](ScorePass& ps, int chunk, int wpad) {
     ps.scored.clear();
     ps.items_per_layer = ps.inst_per_layer = ps.max_chunks = 0;
     ps.chunk = chunk;
@@ -277,7 +260,6 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
     for (const SeqDesc& s0 : p.all) {
       if (C > 0 && s0.len < C) continue;
       SeqDesc s = s0;
-      s.len -= len_cut;
       s.n_chunks = (s.len + chunk - 1) / chunk;
       if (s.n_chunks == 0) continue;  // empty sequence (W <= 0 already rejected)
       s.item_base = ps.items_per_layer;
@@ -292,32 +274,13 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
   if (tc_ok) {
     ScorePass one;
     one.W = W;
-    build(one, tc_chunk_tokens(W), tc_window_pad(W), 0);
+    build(one, tc_chunk_tokens(W), tc_window_pad(W));
     // the waits between the chunks of one instance end only if its chunks
     // span at most three rounds of items (chunks <= 2 x CTAs)
     if (one.max_chunks <= tc_max_chunks(W, d->sm_count)) {
       sp->tc = true;
-      if (allow_split && one.max_chunks > kTwoPassChunks) {
-        one.two_pass = kTwoPassLag;
-        sp->passes.push_back(std::move(one));
-        return KVSEL_OK;
-      }
-      if (allow_split && tc_window_pad(W) == 64 && one.max_chunks > kSplitChunks) {
-        ScorePass a0, a1;
-        a0.W = 32;
-        build(a0, tc_chunk_tokens(32), 32, W - 32);
-        a1.W = W - 32;
-        a1.q_row0 = 32;
-        a1.vote_cut = 32;
-        a1.accumulate = 1;
-        build(a1, tc_chunk_tokens(a1.W), tc_window_pad(a1.W), 0);
-        if (a0.max_chunks <= tc_max_chunks(32, d->sm_count) &&
-            a1.max_chunks <= tc_max_chunks(a1.W, d->sm_count)) {
-          sp->passes.push_back(std::move(a0));
-          sp->passes.push_back(std::move(a1));
-          return KVSEL_OK;
-        }
-      }
+      // (logits mode keeps the one-pass kernel: it stores logits, not votes)
+      if (allow_two_pass && one.max_chunks > kTwoPassChunks) one.two_pass = kTwoPassLag;
       sp->passes.push_back(std::move(one));
       return KVSEL_OK;
     }
@@ -326,7 +289,7 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
   sp->tc = false;
   ScorePass g;
   g.W = W;
-  build(g, kGenericChunk, W, 0);
+  build(g, kGenericChunk, W);
   sp->passes.push_back(std::move(g));
   return KVSEL_OK;
 }
@@ -377,9 +340,6 @@ kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, D
   a.T = p.T;
   a.q_rows = (int64_t)p.S * W;
   a.q_W = W;
-  a.q_row0 = ps.q_row0;
-  a.vote_cut = ps.vote_cut;
-  a.accumulate = ps.accumulate;
   a.two_pass = ps.two_pass;
   a.n_scored = (int)ps.scored.size();
   a.seqs = reinterpret_cast<const SeqDesc*>(ws + o_seq);
@@ -599,7 +559,6 @@ int32_t kvsel_score_path(const kvsel_shape* shape, int32_t W, int32_t C) {
       (reinterpret_cast<uintptr_t>(probe) + 255) & ~uintptr_t(255));
   if (plan_score(p, W, C, aligned, aligned, d, &sp) != KVSEL_OK) return -1;
   if (!sp.tc) return 0;
-  if (sp.passes.size() > 1) return 2;
   return sp.passes[0].two_pass ? 3 : 1;
 }
 

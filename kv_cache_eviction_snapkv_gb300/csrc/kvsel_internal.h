@@ -31,10 +31,7 @@ struct ScoreArgs {
   int kv_group;            // query heads per K head: K head of query head h is h / kv_group
   int64_t T;               // tokens per layer
   int64_t q_rows;          // rows of q_win per layer (num_seqs * q_W)
-  int q_W;                 // window rows per sequence in q_win (W unless the rows are split)
-  int q_row0;              // this pass's first window row within a sequence's q_W rows
-  int vote_cut;            // votes are written for tok < len - W - vote_cut, 0 elsewhere
-  int accumulate;          // 1: add this pass's votes to those already in `votes`
+  int q_W;                 // window rows per sequence in q_win (= W)
   int two_pass;            // > 0: the two-pass kernel for long instances (statistics,
                            // then votes from recomputed logits this many items later)
   int n_scored;            // number of scored sequences

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kThreads) generic_score_kernel(ScoreArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // Stage this (layer, sequence, head)'s W window queries.
-  const int64_t q_row0 = (int64_t)ip.layer * a.q_rows + (int64_t)sd.index * a.q_W + a.q_row0;
+  const int64_t q_row0 = (int64_t)ip.layer * a.q_rows + (int64_t)sd.index * a.q_W;
   for (int e = tid; e < W * D; e += kThreads) {
     int r = e / D, d = e - r * D;
     qs[e] = load_elem(a.q, ((q_row0 + r) * H + ip.h) * D + d, a.dtype);

@@ -502,9 +502,7 @@ __device__ __forceinline__ void stats_warp_loop(const ScoreArgs& a, Misc* ms, in
     if (cp_out[b] && lane == 0) mbar_wait(smem_u32(&ms->slot_bar[b]), cp_par[b], limit, nullptr);
 }
 
-// ACC: add the votes to those already in `votes` (the second pass of a
-// window-row split).
-template <int NW, int KD, bool LOGITS, bool ACC>
+template <int NW, int KD, bool LOGITS>
 __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcParams P) {
   constexpr int kHalves = KD / 64;
   constexpr int kStageBytes = kTileM * KD * 2;
@@ -596,7 +594,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf)
           tma_load_4d(smem_u32(sq + qb * kQBytes + hf * NW * 128), &P.tmq,
-                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h, a.q_row0,
+                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h, 0,
                       ip.layer * seqs_per_layer + sd.index, pol_q);
         q_armed |= 1u << qb;
         q_par = (q_par & ~(1u << qb)) | (qp << qb);
@@ -867,18 +865,6 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
           // log2 Z_r) (the reference of this lane quarter; 0 for padded
           // rows). This warp takes the tiles of parity `sub`, all rows.
           const int64_t plane = ((int64_t)ip.layer * a.H + ip.h) * a.T + sd.tok_off;
-          // ACC: the earlier pass's votes of this warp's tokens, loaded before
-          // the wait for the statistics so that their latency overlaps it
-          constexpr int kTpw = ACC ? tiles_per_item(NW) / 2 : 1;
-          float prev[kTpw];
-          if constexpr (ACC) {
-#pragma unroll
-            for (int u = 0; u < kTpw; ++u) {
-              const int t = sub + 2 * u;
-              const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-              prev[u] = (t < ntiles && tok < prefix - a.vote_cut) ? a.votes[plane + tok] : 0.f;
-            }
-          }
           if (ok)
             ok = __all_sync(0xffffffffu,
                             mbar_wait(smem_u32(&ms->ffull[b]), use, limit, abort_flag));
@@ -887,7 +873,8 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
             cf[r] = r < W ? ex2(ms->wm[b][quarter][r] - ms->fin[b][r]) : 0.f;
           __syncwarp();
           mbar_arrive(smem_u32(&ms->fempty[b]));
-          auto vote_tile = [&](int t, float add) {
+          for (int t = sub; t < ntiles; t += 2) {
+            if (!ok) break;
             float ev[NW];
             tmem_load_row<NW>(item_addr + (uint32_t)(t * NW), ev);
             float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -902,33 +889,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
             const int tok = tok0 + t * kTileM + 32 * quarter + lane;
             if (tok < sd.len)
               a.votes[plane + tok] =
-                  tok < prefix - a.vote_cut ? ((p[0] + p[1]) + (p[2] + p[3])) + add : 0.f;
-          };
-          if constexpr (ACC) {
-#pragma unroll
-            for (int u = 0; u < kTpw; ++u) {
-              const int t = sub + 2 * u;
-              if (ok && t < ntiles) vote_tile(t, prev[u]);
-            }
-          } else {
-            for (int t = sub; t < ntiles; t += 2) {
-              if (!ok) break;
-              float ev[NW];
-              tmem_load_row<NW>(item_addr + (uint32_t)(t * NW), ev);
-              float p[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int i = 0; i < NW; i += 4) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cf + i);
-                p[0] = fmaf(ev[i], c4.x, p[0]);
-                p[1] = fmaf(ev[i + 1], c4.y, p[1]);
-                p[2] = fmaf(ev[i + 2], c4.z, p[2]);
-                p[3] = fmaf(ev[i + 3], c4.w, p[3]);
-              }
-              const int tok = tok0 + t * kTileM + 32 * quarter + lane;
-              if (tok < sd.len)
-                a.votes[plane + tok] =
-                    tok < prefix - a.vote_cut ? (p[0] + p[1]) + (p[2] + p[3]) : 0.f;
-            }
+                  tok < prefix ? (p[0] + p[1]) + (p[2] + p[3]) : 0.f;
           }
           tc_fence_before();
           __syncwarp();
@@ -1083,7 +1044,7 @@ __global__ void __maxnreg__(kRegs) tc_score_rc_kernel(const __grid_constant__ Tc
 #pragma unroll
           for (int hf = 0; hf < kHalves; ++hf)
             tma_load_4d(smem_u32(sq + pass * kQBytes + hf * NW * 128), &P.tmq,
-                        smem_u32(&ms->qfull[pass]), hf * 64, ip.h, a.q_row0,
+                        smem_u32(&ms->qfull[pass]), hf * 64, ip.h, 0,
                         ip.layer * seqs_per_layer + sd.index, pol_q);
           q_armed |= 1u << pass;
           q_par = (q_par & ~(1u << pass)) | (qp << pass);
@@ -1420,7 +1381,7 @@ bool make_qmap(CUtensorMap* m, const void* base, int D, int H, int W, int64_t se
   return r == CUDA_SUCCESS;
 }
 
-template <int NW, int KD, bool LOGITS, bool ACC, bool RC = false>
+template <int NW, int KD, bool LOGITS, bool RC = false>
 cudaError_t launch_t(const ScoreArgs& a, int grid) {
   constexpr int kStageBytes = kTileM * KD * 2;
   constexpr int kQBytes = NW * KD * 2;
@@ -1437,7 +1398,7 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   p.a = a;
   p.stages = stages;
   p.n_items = a.layers * a.items_per_layer;
-  void (*kern)(const TcParams) = RC ? tc_score_rc_kernel<NW, KD> : tc_score_kernel<NW, KD, LOGITS, ACC>;
+  void (*kern)(const TcParams) = RC ? tc_score_rc_kernel<NW, KD> : tc_score_kernel<NW, KD, LOGITS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1457,37 +1418,26 @@ template <bool LOGITS>
 cudaError_t launch_mode(const ScoreArgs& a, int grid) {
   const int nw = tc_window_pad(a.W);
   if (a.two_pass) {  // long instances: statistics and votes in two passes, never logits
-    if (LOGITS || a.accumulate || a.two_pass < 2) return cudaErrorInvalidValue;
-    if (a.D == 128) {
-      if (nw == 16) return launch_t<16, 128, false, false, true>(a, grid);
-      if (nw == 32) return launch_t<32, 128, false, false, true>(a, grid);
-      if (nw == 64) return launch_t<64, 128, false, false, true>(a, grid);
-    } else if (a.D == 64) {
-      if (nw == 16) return launch_t<16, 64, false, false, true>(a, grid);
-      if (nw == 32) return launch_t<32, 64, false, false, true>(a, grid);
-      if (nw == 64) return launch_t<64, 64, false, false, true>(a, grid);
-    }
-    return cudaErrorInvalidValue;
-  }
-  if (a.accumulate) {  // second pass of a split: at most 32 rows, never logits
-    if (LOGITS) return cudaErrorInvalidValue;
+    if (LOGITS || a.two_pass < 2) return cudaErrorInvalidValue;
     if (a.D == 128) {
       if (nw == 16) return launch_t<16, 128, false, true>(a, grid);
       if (nw == 32) return launch_t<32, 128, false, true>(a, grid);
+      if (nw == 64) return launch_t<64, 128, false, true>(a, grid);
     } else if (a.D == 64) {
       if (nw == 16) return launch_t<16, 64, false, true>(a, grid);
       if (nw == 32) return launch_t<32, 64, false, true>(a, grid);
+      if (nw == 64) return launch_t<64, 64, false, true>(a, grid);
     }
     return cudaErrorInvalidValue;
   }
   if (a.D == 128) {
-    if (nw == 16) return launch_t<16, 128, LOGITS, false>(a, grid);
-    if (nw == 32) return launch_t<32, 128, LOGITS, false>(a, grid);
-    if (nw == 64) return launch_t<64, 128, LOGITS, false>(a, grid);
+    if (nw == 16) return launch_t<16, 128, LOGITS>(a, grid);
+    if (nw == 32) return launch_t<32, 128, LOGITS>(a, grid);
+    if (nw == 64) return launch_t<64, 128, LOGITS>(a, grid);
   } else if (a.D == 64) {
-    if (nw == 16) return launch_t<16, 64, LOGITS, false>(a, grid);
-    if (nw == 32) return launch_t<32, 64, LOGITS, false>(a, grid);
-    if (nw == 64) return launch_t<64, 64, LOGITS, false>(a, grid);
+    if (nw == 16) return launch_t<16, 64, LOGITS>(a, grid);
+    if (nw == 32) return launch_t<32, 64, LOGITS>(a, grid);
+    if (nw == 64) return launch_t<64, 64, LOGITS>(a, grid);
   }
   return cudaErrorInvalidValue;
 }

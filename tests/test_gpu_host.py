@@ -43,7 +43,7 @@ CASES = [
     ("bf16", 3, 4, 128, 32, 256, "bf16", "avg", 7, [1000, 300, 2600], True),
     ("bf16_pageable_qk", 2, 2, 64, 16, 128, "bf16", "max", 5, [700, 90, 1500], False),
     ("f32", 2, 3, 64, 8, 64, "f32", "avg", 3, [400, 37, 900], True),
-    ("bf16_w64_split", 1, 2, 128, 64, 1024, "bf16", "avg", 7, [34000, 2000], True),
+    ("bf16_w64_two_pass", 1, 2, 128, 64, 1024, "bf16", "avg", 7, [34000, 2000], True),
 ]
 
 

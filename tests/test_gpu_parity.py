@@ -257,7 +257,7 @@ E2E_CASES = [
     ("bf16_tc_w16_max", 1, 3, 64, 16, 100, "bf16", "max", 5, [2000, 99, 640]),
     ("f32_generic", 1, 4, 64, 32, 256, "f32", "avg", 7, [1024]),
     ("bf16_tc_w64", 1, 2, 128, 64, 300, "bf16", "avg", 3, [5000, 64, 65]),
-    ("bf16_tc_w64_split", 1, 2, 128, 64, 2048, "bf16", "avg", 7, [36000, 3000, 2047]),
+    ("bf16_tc_w64_two_pass", 1, 2, 128, 64, 2048, "bf16", "avg", 7, [36000, 3000, 2047]),
 ]
 
 
