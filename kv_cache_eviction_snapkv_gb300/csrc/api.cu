@@ -390,6 +390,50 @@ kvsel_status upload_all(const Plan& p, char* ws, Carve& cv, cudaStream_t stream,
   return KVSEL_OK;
 }
 
+// Packs the selection's instances (kPackWhole in kvsel_internal.h) when its
+// clusters hold more than one CTA and some instances fit one CTA's slice:
+// whole-cluster instances first (the longest work starts in the first wave),
+// then the others cs to a cluster. Uploads the table; leaves sa->pack null
+// when nothing packs. Instances are numbered ((layer * S) + b) * Hsel + h.
+size_t select_pack_bytes(const Plan& p) {
+  return (size_t)p.layers * p.S * p.H * kSelMaxCluster * sizeof(int32_t) + 256;
+}
+
+kvsel_status select_pack(const Plan& p, int W, int C, int Hsel, char* ws, Carve& cv,
+                         cudaStream_t stream, SelectArgs* sa) {
+  sa->pack = nullptr;
+  sa->n_clusters = 0;
+  int cs = 1, slice = 1;
+  select_geometry(sa->max_prefix, &cs, &slice);
+  if (cs <= 1 || cs > kSelMaxCluster) return KVSEL_OK;
+  std::vector<int32_t> whole, single;
+  for (int layer = 0; layer < p.layers; ++layer)
+    for (int b = 0; b < p.S; ++b) {
+      const SeqDesc& sd = p.all[b];
+      const bool one = sd.len < C || (int64_t)sd.len - W <= slice;
+      for (int h = 0; h < Hsel; ++h)
+        (one ? single : whole).push_back((int32_t)(((int64_t)layer * p.S + b) * Hsel + h));
+    }
+  if (single.empty()) return KVSEL_OK;
+  const size_t nc = whole.size() + (single.size() + cs - 1) / cs;
+  std::vector<int32_t> tab(nc * kSelMaxCluster, -1);
+  size_t c = 0;
+  for (int32_t i : whole) {
+    tab[c * kSelMaxCluster] = i;
+    tab[c * kSelMaxCluster + 1] = kPackWhole;
+    ++c;
+  }
+  for (size_t k = 0; k < single.size(); k += cs, ++c)
+    for (int r = 0; r < cs && k + r < single.size(); ++r) tab[c * kSelMaxCluster + r] = single[k + r];
+  const size_t o = cv.take(tab.size() * sizeof(int32_t));
+  cudaError_t e = cudaMemcpyAsync(ws + o, tab.data(), tab.size() * sizeof(int32_t),
+                                  cudaMemcpyHostToDevice, stream);
+  if (e) return cuda_fail(e, "cudaMemcpyAsync(selection packing)");
+  sa->pack = reinterpret_cast<const int32_t*>(ws + o);
+  sa->n_clusters = (int)nc;
+  return KVSEL_OK;
+}
+
 size_t score_ws_bytes(const Plan& p, const ScorePlan& sp) {
   size_t total = 4096;
   for (const ScorePass& ps : sp.passes) {
@@ -636,7 +680,8 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   DevState* d;
   if ((st = device_state(&d))) return st;
   char* ws;
-  if ((st = workspace(d, p.all.size() * sizeof(SeqDesc) + 1024, &ws))) return st;
+  if ((st = workspace(d, p.all.size() * sizeof(SeqDesc) + select_pack_bytes(p) + 1024, &ws)))
+    return st;
   Carve cv;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const SeqDesc* all_dev;
@@ -660,6 +705,7 @@ kvsel_status kvsel_select(const kvsel_shape* shape, const float* pooled, int32_t
   sa.kv_H = p.H;
   sa.kv_div = 1;
   sa.stream = s;
+  if ((st = select_pack(p, W, C, sa.H, ws, cv, s, &sa))) return st;
   return cuda_fail(launch_select(sa), "selection launch");
 }
 
@@ -900,7 +946,8 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
   char* ws;
   if ((st = workspace(d, score_ws_bytes(p, sp) + plane_bytes + 2 * 256 +
-                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) + 1024,
+                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) +
+                             select_pack_bytes(p) + 1024,
                       &ws)))
     return st;
   Carve cv;
@@ -938,6 +985,7 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   sa.out_v = out_V;
   sa.row_bytes = (int64_t)p.D * p.elem_bytes;
   sa.stream = s;
+  if ((st = select_pack(p, W, C, sa.H, ws, cv, s, &sa))) return st;
   if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
   if (ev) {
     cudaEventRecord(ev[2], s);
@@ -992,7 +1040,8 @@ kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void
   const JacapPlan jp = plan_jacap(p, W, C, d->sm_count);
   char* ws;
   if ((st = workspace(d, jacap_ws_bytes(p, jp) + plane_bytes + 2 * 256 +
-                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) + 1024,
+                             kSchedWords * sizeof(int) + p.all.size() * sizeof(SeqDesc) +
+                             select_pack_bytes(p) + 1024,
                       &ws)))
     return st;
   Carve cv;
@@ -1029,6 +1078,7 @@ kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void
   sa.out_v = out_V;
   sa.row_bytes = (int64_t)p.D * p.elem_bytes;
   sa.stream = s;
+  if ((st = select_pack(p, W, C, sa.H, ws, cv, s, &sa))) return st;
   if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
   if (ev) {
     cudaEventRecord(ev[2], s);

@@ -87,6 +87,9 @@ struct SelectArgs {
   void* out_v;
   int64_t row_bytes;       // gather: D * element bytes
   int vec_bytes;           // gather: copy width (set by the launcher)
+  const int32_t* pack;     // null: one instance per cluster in instance order; else the
+                           // packing above, n_clusters clusters
+  int n_clusters;
   int* sched;              // one-CTA instances with the gather: kSchedWords ints zeroed
                            // before the launch (null: no stagger)
   unsigned long long stagger_limit_ns;  // longest hold-back of an SM's second CTA
@@ -206,6 +209,26 @@ constexpr int kJGramMinTiles = 8;    // fewest tiles per Gram CTA (below that, f
 
 constexpr int kMaxSelect = 16384;    // largest C - W the select kernel sorts on chip
 constexpr int64_t kMaxPrefix = 262144;  // longest prefix L - W the select kernel takes
+constexpr int kSelSliceCap = 16384;  // prefix positions one selection CTA holds
+constexpr int kSelMaxCluster = 8;    // selection CTAs per cluster (portable size)
+
+// Selection geometry: CTAs per cluster and prefix positions per CTA for the
+// longest selected prefix.
+inline void select_geometry(int64_t max_prefix, int* cs, int* slice) {
+  int c = (int)((max_prefix + kSelSliceCap - 1) / kSelSliceCap);
+  if (c < 1) c = 1;
+  int sl = (int)((max_prefix + c - 1) / c);
+  *cs = c;
+  *slice = sl < 1 ? 1 : sl;
+}
+
+// Selection packing of ragged batches (launches of clusters of cs > 1 CTAs):
+// an instance whose prefix fits one CTA's slice (or that keeps everything)
+// runs on a single CTA, so cs of them share a cluster; longer instances take
+// a whole cluster. pack[c * kSelMaxCluster + r] for cluster c: either the
+// instance at r = 0 and kPackWhole at r = 1, or the instance of CTA rank r
+// (-1: that CTA has none).
+constexpr int kPackWhole = -2;
 constexpr int kGenericChunk = 256;   // tokens per CUDA-core scoring block
 constexpr int kGenericMaxQ = 16384;  // W * D floats staged in shared memory
 

@@ -26,7 +26,6 @@ namespace {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kMaxCluster = 8;   // portable cluster size
 
 // Order-keeping key: larger float -> larger key; -0 == +0; NaN lowest.
 __device__ __forceinline__ uint32_t score_key(float v, int* status) {
@@ -249,7 +248,7 @@ __device__ void bitonic_sort_blocked(unsigned long long* buf, int nt) {
 struct SelShared {
   uint32_t hist[kBins];        // this CTA's histogram
   uint32_t res[2];             // leader: (bin, count above)
-  uint32_t cnt[kMaxCluster][2];  // leader: per rank (greater, equal) counts
+  uint32_t cnt[kSelMaxCluster][2];  // leader: per rank (greater, equal) counts
   uint32_t warp_cnt[kSelWarps][2];
   uint32_t wsum[kSelWarps];
 };
@@ -1066,6 +1065,20 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm<R>) select_kernel(c
     __syncthreads();
     if (s_slot == 0) selected = flag;
   }
+  if constexpr (!CS1) {
+    if (a.pack) {
+      // a whole-cluster instance, or one single-CTA instance per CTA (block
+      // barriers only: no CTA touches another's shared memory)
+      const uint32_t rank = cluster_rank();
+      const int32_t* e = a.pack + (int64_t)(blockIdx.x / a.cluster) * kSelMaxCluster;
+      if (e[1] == kPackWhole) {
+        select_instance<R, false>(a, e[0], rank, smem, sh, a.gather != 0, nullptr);
+      } else if (e[rank] >= 0) {
+        select_instance<R, true>(a, e[rank], 0u, smem, sh, a.gather != 0, nullptr);
+      }
+      return;
+    }
+  }
   select_instance<R, CS1>(a, blockIdx.x / a.cluster, CS1 ? 0u : cluster_rank(), smem, sh,
                           a.gather != 0, selected);
 }
@@ -1085,13 +1098,13 @@ cudaError_t launch_select(const SelectArgs& a0) {
   SelectArgs a = a0;
   // one CTA per instance up to kSelThreads * kMaxE prefix positions, else a
   // cluster of CTAs with equal slices
-  const int64_t cap = (int64_t)kSelThreads * kMaxE;
-  int cs = (int)((a.max_prefix + cap - 1) / cap);
-  if (cs < 1) cs = 1;
-  if (cs > kMaxCluster) return cudaErrorInvalidValue;
+  static_assert(kSelThreads * kMaxE == kSelSliceCap, "selection slice capacity");
+  int cs = 1, slice = 1;
+  select_geometry(a.max_prefix, &cs, &slice);
+  if (cs > kSelMaxCluster) return cudaErrorInvalidValue;
+  if (a.pack && cs == 1) return cudaErrorInvalidValue;
   a.cluster = cs;
-  a.slice = (int)((a.max_prefix + cs - 1) / cs);
-  if (a.slice < 1) a.slice = 1;
+  a.slice = slice;
   int n2 = kSelThreads;
   while (n2 < a.C - a.W) n2 <<= 1;
   const int pad = a.pool_inline ? a.pool_k / 2 : 0;
@@ -1131,7 +1144,7 @@ cudaError_t launch_select(const SelectArgs& a0) {
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
     return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(blocks * cs));
+  cfg.gridDim = dim3((unsigned)((a.pack ? (int64_t)a.n_clusters : blocks) * cs));
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
