@@ -956,7 +956,10 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
   float* votes = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
   cudaEvent_t* ev = profile_slot();
-  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s, ev))) return st;
+  // the selection's stagger words and packing go out before the scoring, so
+  // the selection kernel directly follows the scoring kernel on the stream
+  // (a programmatic dependent launch: its CTAs may start as the scoring CTAs
+  // leave and wait for the scoring grid's memory before reading the votes)
   SelectArgs sa{};
   if ((st = stagger_words(ws, cv, s, &sa))) return st;
   sa.scores = votes;
@@ -985,7 +988,9 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   sa.out_v = out_V;
   sa.row_bytes = (int64_t)p.D * p.elem_bytes;
   sa.stream = s;
+  sa.pdl = 1;
   if ((st = select_pack(p, W, C, sa.H, ws, cv, s, &sa))) return st;
+  if ((st = run_score(p, sp, d, q_win, K, W, votes, nullptr, ws, cv, s, ev))) return st;
   if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
   if (ev) {
     cudaEventRecord(ev[2], s);
@@ -1050,8 +1055,8 @@ kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void
   if ((st = upload_all(p, ws, cv, s, &all_dev))) return st;
   float* scores = reinterpret_cast<float*>(ws + cv.take(plane_bytes));
   cudaEvent_t* ev = profile_slot();
-  if ((st = run_jacap(p, jp, d, q_win, K, V, W, tau, beta, eps, scores, ws, cv, s, ev)))
-    return st;
+  // selection set-up first, so the selection kernel directly follows the
+  // scoring kernels (programmatic dependent launch, as in the SnapKV path)
   SelectArgs sa{};
   if ((st = stagger_words(ws, cv, s, &sa))) return st;
   sa.scores = scores;
@@ -1078,7 +1083,10 @@ kvsel_status kvsel_jacap(const kvsel_shape* shape, const void* q_win, const void
   sa.out_v = out_V;
   sa.row_bytes = (int64_t)p.D * p.elem_bytes;
   sa.stream = s;
+  sa.pdl = 1;
   if ((st = select_pack(p, W, C, sa.H, ws, cv, s, &sa))) return st;
+  if ((st = run_jacap(p, jp, d, q_win, K, V, W, tau, beta, eps, scores, ws, cv, s, ev)))
+    return st;
   if ((st = cuda_fail(launch_select(sa), "selection and gather launch"))) return st;
   if (ev) {
     cudaEventRecord(ev[2], s);

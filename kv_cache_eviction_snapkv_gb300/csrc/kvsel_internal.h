@@ -90,6 +90,8 @@ struct SelectArgs {
   const int32_t* pack;     // null: one instance per cluster in instance order; else the
                            // packing above, n_clusters clusters
   int n_clusters;
+  int pdl;                 // 1: launched as a programmatic dependent of the preceding
+                           // kernel on the stream (its CTAs wait for that grid's memory)
   int* sched;              // one-CTA instances with the gather: kSchedWords ints zeroed
                            // before the launch (null: no stagger)
   unsigned long long stagger_limit_ns;  // longest hold-back of an SM's second CTA

@@ -1048,6 +1048,10 @@ template <int R, bool CS1>
 __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm<R>) select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ SelShared sh;
+  // a programmatic dependent launch may start before the scoring grid is
+  // done: wait for it (and its memory) before reading any score (returns at
+  // once when the launch has no such dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int* selected = nullptr;
   if (CS1 && a.sched && a.gather) {
     __shared__ int s_slot;
@@ -1148,13 +1152,15 @@ cudaError_t launch_select(const SelectArgs& a0) {
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
