@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--no-decode", action="store_true",
                    help="skip the decode-consumer measurement")
     p.add_argument("--no-jacap", action="store_true", help="skip the Jacap measurement")
+    p.add_argument("--no-gqa", action="store_true",
+                   help="skip the grouped-query (group-shared selection) measurement")
     p.add_argument("--no-reverse", action="store_true",
                    help="skip the reverse-mask attention measurement")
     p.add_argument("--no-cpu", action="store_true")
@@ -385,6 +387,66 @@ def measure_jacap(api, wl, q_win, k, v, dev, peak, peak_kind, iters=10):
             "fused_ms": ms_full, "fused_head_tokens_per_s": wl.head_tokens() / (ms_full * 1e-3)}
 
 
+def measure_gqa(api, wk, dev, peak, peak_kind, iters=20):
+    """Group-shared selection with grouped-query attention: 4 layers, 32 query
+    heads over 8 K/V heads, L = 16384, D = 128, W = 16, C = 2048, bf16 N(0,1),
+    average pooling 7 (inputs larger than L2). kvsel_snapkv_grouped scores the
+    four query heads of a K/V head in one MMA (64 window rows), reading K once
+    per K/V head; kvsel_snapkv on the same inputs selects per query head and
+    reads each K row once per query head. CUDA events on the launching stream."""
+    import torch
+    lens = [16384]
+    wq = wk.custom_workload("gqa_q", 4, 32, 128, 16, 2048, "bf16", "avg", 7, lens, 2101)
+    wkv = wk.custom_workload("gqa_kv", 4, 8, 128, 16, 2048, "bf16", "avg", 7, lens, 2102)
+    q, _, _ = wk.device_tensors(wq, dev)
+    _, k, v = wk.device_tensors(wkv, dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        api.kvsel_profile_begin(iters)
+        for _ in range(iters):
+            fn()
+        stage_ms, calls = api.kvsel_profile_end()
+        return ms, stage_ms[0] / calls, stage_ms[1] / calls
+
+    offs = wq.offsets
+    ms_g, score_g, sel_g = timed(lambda: api.kvsel_snapkv_grouped(q, k, v, offs, 16, 2048, 0, 7))
+    ms_e, score_e, sel_e = timed(lambda: api.kvsel_snapkv(q, k, v, offs, 16, 2048, 0, 7))
+    st = api.kvsel_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after GQA: {api.kvsel_status_string(st)}")
+    row = 128 * 2
+    L, layers, hq, hkv = 16384, 4, 32, 8
+    qbytes = layers * hq * 16 * row
+    # group-shared: K once per K/V head, the kept K/V rows of each K/V head read and written
+    k_bytes = layers * hkv * L * row
+    b_g = k_bytes + qbytes + layers * hkv * 4 * 2048 * row
+    del q, k, v
+    torch.cuda.empty_cache()
+    return {"workload": "4 layers, 32 query heads over 8 K/V heads, L = 16384, D = 128, W = 16, "
+                        "C = 2048, bf16 N(0,1), avg pooling 7",
+            "grouped": {"entry": "kvsel_snapkv_grouped (one MMA per K tile for the 4 query "
+                                 "heads of a group)",
+                        "ms": ms_g, "score_ms": score_g, "select_gather_ms": sel_g,
+                        "bytes": b_g, "achieved_gbs": b_g / (ms_g * 1e-3) / 1e9,
+                        "frac": b_g / (ms_g * 1e-3) / 1e9 / peak,
+                        "score_gbs": (k_bytes + qbytes) / (score_g * 1e-3) / 1e9,
+                        "score_frac": (k_bytes + qbytes) / (score_g * 1e-3) / 1e9 / peak},
+            "per_query_head": {"entry": "kvsel_snapkv (K read once per query head)",
+                               "ms": ms_e, "score_ms": score_e, "select_gather_ms": sel_e},
+            "peak": peak, "peak_source": peak_kind, "unit": "GB/s"}
+
+
 def measure_reverse(api, dev, iters=10):
     """Reverse-mask attention of the counter-causal scorer on the shape the
     page times (one sequence of n cached rows, 28 query heads over 4 K/V heads,
@@ -639,6 +701,11 @@ def main():
     if not args.no_jacap and wl.dtype == "bf16" and wl.dim == 128:
         jacap = measure_jacap(api, wl, q, k, v, dev, peak, peak_kind)
 
+    # Grouped-query attention, group-shared selection (its own inputs).
+    gqa = None
+    if not args.no_gqa and rank == 0:
+        gqa = measure_gqa(api, wk, dev, peak, peak_kind)
+
     # Reverse-mask attention of the counter-causal scorer (its own inputs).
     reverse = None
     if not args.no_reverse and rank == 0:
@@ -729,6 +796,7 @@ def main():
             "decode": decode,
             "jacap": jacap,
             "reverse": reverse,
+            "gqa": gqa,
             "configs": configs,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,

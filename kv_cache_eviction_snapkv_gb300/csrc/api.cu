@@ -229,6 +229,8 @@ struct ScorePass {
   int chunk = 0, wpad = 0;
   int W = 0;           // window rows (the causal mask and statistics)
   int two_pass = 0;    // > 0: the two-pass kernel with this lag (long instances)
+  int qg = 1;          // query heads scored together per K/V head (group-shared
+                       // selection on the tensor cores); instances are then K/V heads
 };
 
 struct ScorePlan {
@@ -249,10 +251,16 @@ struct ScorePlan {
 constexpr int kTwoPassChunks = KVSEL_TWO_PASS_CHUNKS;
 constexpr int kTwoPassLag = KVSEL_TWO_PASS_LAG;
 
+// `group` > 1 (the group-shared selection): where the one-pass tensor-core
+// kernel can take the group's G * W window rows at once (G a power of two,
+// G * W <= 64), each K/V head is scored once against its G query heads and
+// the votes come out summed per K/V head (sp->passes[0].qg = G); otherwise
+// every query head is scored on its own.
 kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* k,
-                        const DevState* d, ScorePlan* sp, bool allow_two_pass = true) {
+                        const DevState* d, ScorePlan* sp, bool allow_two_pass = true,
+                        int group = 1) {
   const bool tc_ok = d->cc_major == 10 && tc_eligible(p.dtype, p.D, W, q, k);
-  auto build = [&](ScorePass& ps, int chunk, int wpad) {
+  auto build = [&](ScorePass& ps, int chunk, int wpad, int heads) {
     ps.scored.clear();
     ps.items_per_layer = ps.inst_per_layer = ps.max_chunks = 0;
     ps.chunk = chunk;
@@ -264,17 +272,29 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
       if (s.n_chunks == 0) continue;  // empty sequence (W <= 0 already rejected)
       s.item_base = ps.items_per_layer;
       s.inst_base = ps.inst_per_layer;
-      ps.items_per_layer += p.H * s.n_chunks;
-      ps.inst_per_layer += p.H;
+      ps.items_per_layer += heads * s.n_chunks;
+      ps.inst_per_layer += heads;
       if (s.n_chunks > ps.max_chunks) ps.max_chunks = s.n_chunks;
       ps.scored.push_back(s);
     }
   };
   sp->passes.clear();
+  if (tc_ok && group > 1 && (group & (group - 1)) == 0 && group * W <= 64 &&
+      tc_eligible(p.dtype, p.D, group * W, q, k)) {
+    ScorePass gp;
+    gp.W = W;
+    gp.qg = group;
+    build(gp, tc_chunk_tokens(group * W), tc_window_pad(group * W), p.H / group);
+    if (gp.max_chunks <= std::min(tc_max_chunks(group * W, d->sm_count), kTwoPassChunks)) {
+      sp->tc = true;
+      sp->passes.push_back(std::move(gp));
+      return KVSEL_OK;
+    }
+  }
   if (tc_ok) {
     ScorePass one;
     one.W = W;
-    build(one, tc_chunk_tokens(W), tc_window_pad(W));
+    build(one, tc_chunk_tokens(W), tc_window_pad(W), p.H);
     // the waits between the chunks of one instance end only if its chunks
     // span at most three rounds of items (chunks <= 2 x CTAs)
     if (one.max_chunks <= tc_max_chunks(W, d->sm_count)) {
@@ -289,7 +309,7 @@ kvsel_status plan_score(const Plan& p, int W, int C, const void* q, const void* 
   sp->tc = false;
   ScorePass g;
   g.W = W;
-  build(g, kGenericChunk, W);
+  build(g, kGenericChunk, W, p.H);
   sp->passes.push_back(std::move(g));
   return KVSEL_OK;
 }
@@ -332,8 +352,9 @@ kvsel_status run_pass(const Plan& p, const ScorePlan& sp, const ScorePass& ps, D
   a.q = q;
   a.k = k;
   a.layers = p.layers;
-  a.H = p.H;
-  a.kv_group = p.G;
+  a.H = p.H / ps.qg;            // instance heads
+  a.kv_group = ps.qg > 1 ? 1 : p.G;
+  a.qg = ps.qg;
   a.D = p.D;
   a.dtype = p.dtype;
   a.W = ps.W;
@@ -942,7 +963,9 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   DevState* d;
   if ((st = device_state(&d))) return st;
   ScorePlan sp;
-  if ((st = plan_score(p, W, C, q_win, K, d, &sp))) return st;
+  if ((st = plan_score(p, W, C, q_win, K, d, &sp, true, grouped ? p.G : 1))) return st;
+  // group-shared scoring writes one vote plane per K/V head, already summed
+  const bool group_scored = !sp.passes.empty() && sp.passes[0].qg > 1;
   const size_t plane_bytes = (size_t)p.layers * p.H * p.T * sizeof(float);
   char* ws;
   if ((st = workspace(d, score_ws_bytes(p, sp) + plane_bytes + 2 * 256 +
@@ -968,7 +991,7 @@ kvsel_status snapkv_impl(const kvsel_shape* shape, const void* q_win, const void
   sa.pool_k = pool_k;
   sa.layers = p.layers;
   sa.H = grouped ? p.Hkv : p.H;
-  sa.vote_group = grouped ? p.G : 1;
+  sa.vote_group = grouped && !group_scored ? p.G : 1;
   sa.kv_H = p.Hkv;
   sa.kv_div = grouped ? 1 : p.G;
   sa.W = W;

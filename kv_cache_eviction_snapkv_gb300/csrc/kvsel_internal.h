@@ -29,6 +29,10 @@ struct ScoreArgs {
   const void* k;           // K
   int layers, H, D, dtype, W;
   int kv_group;            // query heads per K head: K head of query head h is h / kv_group
+  int qg;                  // query heads scored together against one K head (tensor-core
+                           // one-pass kernel, group-shared selection): instance head h
+                           // takes query heads h * qg .. h * qg + qg - 1 as qg * W window
+                           // rows (row w * qg + g); 1 otherwise
   int64_t T;               // tokens per layer
   int64_t q_rows;          // rows of q_win per layer (num_seqs * q_W)
   int q_W;                 // window rows per sequence in q_win (= W)

@@ -253,7 +253,7 @@ template <int NW>
 __device__ __forceinline__ void stats_warp_loop(const ScoreArgs& a, Misc* ms, int n_my, int G,
                                                 int lane, unsigned long long limit,
                                                 volatile int* abort_flag, int owner_ahead) {
-  const int W = a.W;
+  const int W = a.W * a.qg;   // window rows of an instance (qg query heads of W rows)
   constexpr int kStageSlots = slot_stage_for(NW) / 16;   // per staging buffer
   const unsigned long long* part = reinterpret_cast<const unsigned long long*>(a.part);
   unsigned long long* fslots = reinterpret_cast<unsigned long long*>(a.final_stats);
@@ -513,6 +513,10 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
   const ScoreArgs& a = P.a;
   const int stages = P.stages;
   const int W = a.W;
+  // qg query heads share the instance's K: window row r of the tile is query
+  // offset r / qg of head r % qg; R rows are valid
+  const int qg = a.qg;
+  const int R = W * qg;
   const int G = gridDim.x;
   // this CTA's items: blockIdx.x + it * G, it = 0 .. n_my - 1
   const int n_my = P.n_items > (int)blockIdx.x ? (P.n_items - 1 - (int)blockIdx.x) / G + 1 : 0;
@@ -594,7 +598,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf)
           tma_load_4d(smem_u32(sq + qb * kQBytes + hf * NW * 128), &P.tmq,
-                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h, 0,
+                      smem_u32(&ms->qfull[qb]), hf * 64, ip.h * qg, 0,
                       ip.layer * seqs_per_layer + sd.index, pol_q);
         q_armed |= 1u << qb;
         q_par = (q_par & ~(1u << qb)) | (qp << qb);
@@ -780,9 +784,9 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
               tmem_store_cols<NH>(taddr, y);
             } else {
               // window tokens and the ragged tail, eight rows at a time: rows
-              // visible to this token are row0 + i < W with tok <= P + row0 + i
-              const int lo = max(0, tok - prefix - row0);
-              const int hi = tok < sd.len ? min(NH, W - row0) : 0;
+              // visible to this token are row0 + i < R with tok <= P + (row0 + i) / qg
+              const int lo = max(0, (tok - prefix) * qg - row0);
+              const int hi = tok < sd.len ? min(NH, R - row0) : 0;
 #pragma unroll
               for (int cb = 0; cb < NH; cb += 8) {
                 float xb[8];
@@ -833,7 +837,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
             tmem_wait_st();
 #pragma unroll
             for (int i = 0; i < NH; ++i)
-              if (row0 + i < W && zsum[i] != zsum[i]) bad = true;
+              if (row0 + i < R && zsum[i] != zsum[i]) bad = true;
             if (ymin == -INFINITY) bad = true;
             if (bad) record_status(a.status, KVSEL_ERR_NONFINITE);
             reduce_sum<NH>(zsum, lane);
@@ -847,7 +851,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
             epi_bar();
             tc_fence_after();
             if (warp == kEpiWarp0) {
-              for (int r = lane; r < W; r += 32) {
+              for (int r = lane; r < R; r += 32) {
                 float m = ms->wm[b][0][r], z = ms->wz[b][0][r];
 #pragma unroll
                 for (int q = 1; q < 4; ++q) merge_stats(m, z, ms->wm[b][q][r], ms->wz[b][q][r]);
@@ -870,7 +874,7 @@ __global__ void __maxnreg__(kRegs) tc_score_kernel(const __grid_constant__ TcPar
                             mbar_wait(smem_u32(&ms->ffull[b]), use, limit, abort_flag));
           float* cf = ms->cf[e];
           for (int r = lane; r < NW; r += 32)
-            cf[r] = r < W ? ex2(ms->wm[b][quarter][r] - ms->fin[b][r]) : 0.f;
+            cf[r] = r < R ? ex2(ms->wm[b][quarter][r] - ms->fin[b][r]) : 0.f;
           __syncwarp();
           mbar_arrive(smem_u32(&ms->fempty[b]));
           for (int t = sub; t < ntiles; t += 2) {
@@ -1365,15 +1369,17 @@ bool make_kmap(CUtensorMap* m, const void* base, int D, int H, int64_t rows) {
   return r == CUDA_SUCCESS;
 }
 
-// q_win as (D, H, W, layers * S): a box of NW >= W window rows reads rows
-// W .. NW - 1 as zeros (outside the tensor), so padded rows never see another
-// sequence's queries.
-bool make_qmap(CUtensorMap* m, const void* base, int D, int H, int W, int64_t seqs, int nw) {
+// q_win as (D, H, W, layers * S): a box of qg heads x NW / qg window rows
+// (row w * qg + g of the tile is row w of head g) reads rows W .. NW/qg - 1 as
+// zeros (outside the tensor), so padded rows never see another sequence's
+// queries.
+bool make_qmap(CUtensorMap* m, const void* base, int D, int H, int W, int64_t seqs, int nw,
+               int qg) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)W, (cuuint64_t)seqs};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)W * H * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)nw, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)qg, (cuuint32_t)(nw / qg), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1393,7 +1399,8 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   if (!make_kmap(&p.tmk, a.k, a.D, a.H / a.kv_group, (int64_t)a.layers * a.T) ||
-      !make_qmap(&p.tmq, a.q, a.D, a.H, a.q_W, (int64_t)a.layers * (a.q_rows / a.q_W), NW))
+      !make_qmap(&p.tmq, a.q, a.D, a.H * a.qg, a.q_W, (int64_t)a.layers * (a.q_rows / a.q_W), NW,
+                 a.qg))
     return cudaErrorInvalidValue;
   p.a = a;
   p.stages = stages;
@@ -1416,7 +1423,8 @@ cudaError_t launch_t(const ScoreArgs& a, int grid) {
 
 template <bool LOGITS>
 cudaError_t launch_mode(const ScoreArgs& a, int grid) {
-  const int nw = tc_window_pad(a.W);
+  const int nw = tc_window_pad(a.W * a.qg);
+  if (a.qg > 1 && (a.two_pass || LOGITS || nw % a.qg)) return cudaErrorInvalidValue;
   if (a.two_pass) {  // long instances: statistics and votes in two passes, never logits
     if (LOGITS || a.two_pass < 2) return cudaErrorInvalidValue;
     if (a.D == 128) {

@@ -105,7 +105,16 @@ def test_repeat_mode_votes_per_query_head():
                                        atol=VOTE_RTOL * ref["votes"].max())
 
 
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+# group-shared scoring on the tensor cores (the G query heads of a K/V head as
+# G * W <= 64 window rows of one MMA): ragged lengths, bypass, padded rows
+GROUP_CASES = CASES + [
+    ("g4_w16_d128", 1, 8, 2, 128, 16, 300, "bf16", "avg", 7, [3000, 150, 5100]),
+    ("g2_w24_d64", 2, 4, 2, 64, 24, 200, "bf16", "max", 5, [1000, 2333]),
+    ("g8_w8_d128", 1, 16, 2, 128, 8, 100, "bf16", "avg", 3, [900, 1700]),
+]
+
+
+@pytest.mark.parametrize("case", GROUP_CASES, ids=[c[0] for c in GROUP_CASES])
 def test_grouped_mode_matches_oracle(case):
     ensure_built()
     name, layers, hq, hkv, D, W, C, dtype, pool, kk, lens = case
@@ -174,16 +183,18 @@ def test_compact_expands_kv_heads():
             assert torch.equal(ov[:, b * C:(b + 1) * C, h], V[ll, rows[:, :, h], h // 2])
 
 
-def test_grouped_full_size_sampled():
-    """32 query heads on 8 K/V heads, L = 16384, W = 32, C = 2048 (the 32-layer
-    shape's per-layer size): structure everywhere, the oracle on sampled groups."""
+@pytest.mark.parametrize("W", [32, 16])
+def test_grouped_full_size_sampled(W):
+    """32 query heads on 8 K/V heads, L = 16384, C = 2048 (the 32-layer shape's
+    per-layer size; W = 16 puts the four query heads of a group in one MMA):
+    structure everywhere, the oracle on sampled groups."""
     ensure_built()
-    wq, wkv, q, k, v = make("gfull", 1, 32, 8, 128, 32, 2048, "bf16", "avg", 7, [16384], 71)
-    out_idx, out_k, out_v = api().kvsel_snapkv_grouped(q, k, v, wq.offsets, 32, 2048, 0, 7)
+    wq, wkv, q, k, v = make("gfull", 1, 32, 8, 128, W, 2048, "bf16", "avg", 7, [16384], 71)
+    out_idx, out_k, out_v = api().kvsel_snapkv_grouped(q, k, v, wq.offsets, W, 2048, 0, 7)
     assert_ok()
-    n_keep = 2048 - 32
+    n_keep = 2048 - W
     kept = out_idx[0, :n_keep].long()
-    assert int(kept.min()) >= 0 and int(kept.max()) < 16384 - 32
+    assert int(kept.min()) >= 0 and int(kept.max()) < 16384 - W
     srt = torch.sort(kept, dim=0).values
     assert bool((srt[1:] != srt[:-1]).all())
     idx = out_idx.cpu().numpy()
