@@ -1044,7 +1044,7 @@ __device__ void select_instance(const SelectArgs& a, int inst, uint32_t rank,
 // its instance; from then on one CTA of the pair tends to select while the
 // other copies. The wait is on a CTA that is already running and is bounded
 // (running out of time only costs speed).
-template <int R, bool CS1>
+template <int R, bool CS1, bool PACK = false>
 __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm<R>) select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ SelShared sh;
@@ -1069,22 +1069,22 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm<R>) select_kernel(c
     __syncthreads();
     if (s_slot == 0) selected = flag;
   }
-  if constexpr (!CS1) {
-    if (a.pack) {
-      // a whole-cluster instance, or one single-CTA instance per CTA (block
-      // barriers only: no CTA touches another's shared memory)
-      const uint32_t rank = cluster_rank();
-      const int32_t* e = a.pack + (int64_t)(blockIdx.x / a.cluster) * kSelMaxCluster;
-      if (e[1] == kPackWhole) {
-        select_instance<R, false>(a, e[0], rank, smem, sh, a.gather != 0, nullptr);
-      } else if (e[rank] >= 0) {
-        select_instance<R, true>(a, e[rank], 0u, smem, sh, a.gather != 0, nullptr);
-      }
-      return;
+  if constexpr (PACK) {
+    // packed launch (a separate instantiation, so that the plain cluster
+    // kernel keeps its registers): a whole-cluster instance, or one
+    // single-CTA instance per CTA (block barriers only: no CTA touches
+    // another's shared memory)
+    const uint32_t rank = cluster_rank();
+    const int32_t* e = a.pack + (int64_t)(blockIdx.x / a.cluster) * kSelMaxCluster;
+    if (e[1] == kPackWhole) {
+      select_instance<R, false>(a, e[0], rank, smem, sh, a.gather != 0, nullptr);
+    } else if (e[rank] >= 0) {
+      select_instance<R, true>(a, e[rank], 0u, smem, sh, a.gather != 0, nullptr);
     }
+  } else {
+    select_instance<R, CS1>(a, blockIdx.x / a.cluster, CS1 ? 0u : cluster_rank(), smem, sh,
+                            a.gather != 0, selected);
   }
-  select_instance<R, CS1>(a, blockIdx.x / a.cluster, CS1 ? 0u : cluster_rank(), smem, sh,
-                          a.gather != 0, selected);
 }
 
 }  // namespace
@@ -1123,8 +1123,11 @@ cudaError_t launch_select(const SelectArgs& a0) {
   const size_t sortbuf = std::max(merge ? merge_bytes : (size_t)n2 * 8, (size_t)kBins * 4);
   const size_t smem = stage + sortbuf;
   void (*kern)(const SelectArgs) = nullptr;
-#define KVSEL_SEL_CASE(RR) \
-  case RR: kern = cs == 1 ? select_kernel<RR, true> : select_kernel<RR, false>; break;
+#define KVSEL_SEL_CASE(RR)                                                           \
+  case RR:                                                                           \
+    kern = cs == 1 ? select_kernel<RR, true>                                         \
+                   : (a.pack ? select_kernel<RR, false, true> : select_kernel<RR, false>); \
+    break;
   switch (n2 / kSelThreads) {
     KVSEL_SEL_CASE(1)
     KVSEL_SEL_CASE(2)
