@@ -195,8 +195,11 @@ kvsel_status kvsel_snapkv(const kvsel_shape* shape, const void* q_win, const voi
  * group, so the kept cache has H_kv heads (the page leaves this design open;
  * our reading): each query head computes its own causal-softmax votes against
  * the group's keys, the group's vote of a prefix position is the sum of its
- * G heads' votes (in head order), and pooling, the top-(C - W) selection and
- * the gather then run once per group. Layouts: q_win [num_layers][S * W][H][D],
+ * G heads' votes, and pooling, the top-(C - W) selection and the gather then
+ * run once per group. On the tensor cores with G a power of two and G * W <=
+ * 64 the G heads are scored together (K read once per group; the sum is then
+ * taken over all G * W rows at once, equal to the head-ordered sum within
+ * fp32 rounding). Layouts: q_win [num_layers][S * W][H][D],
  * K and V [num_layers][T][H_kv][D]; out_idx [num_layers][T_out][H_kv] int32,
  * out_K and out_V [num_layers][T_out][H_kv][D]. Rules and limits those of
  * kvsel_snapkv. With H_kv == H it is kvsel_snapkv. */
