@@ -258,6 +258,9 @@ E2E_CASES = [
     ("f32_generic", 1, 4, 64, 32, 256, "f32", "avg", 7, [1024]),
     ("bf16_tc_w64", 1, 2, 128, 64, 300, "bf16", "avg", 3, [5000, 64, 65]),
     ("bf16_tc_w64_two_pass", 1, 2, 128, 64, 2048, "bf16", "avg", 7, [36000, 3000, 2047]),
+    # every sequence shorter than C: no scoring launch, the selection (a programmatic
+    # dependent launch) follows the set-up copies directly
+    ("all_bypass", 2, 3, 64, 16, 256, "bf16", "avg", 7, [100, 37, 255]),
 ]
 
 
