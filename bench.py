@@ -21,6 +21,7 @@ the headline's timed region, under the key "configs".
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import multiprocessing as mp
@@ -53,6 +54,9 @@ def parse_args():
     p.add_argument("--no-decode", action="store_true",
                    help="skip the decode-consumer measurement")
     p.add_argument("--no-jacap", action="store_true", help="skip the Jacap measurement")
+    p.add_argument("--split", action="store_true",
+                   help="with several GPUs, split the workload's layers over the ranks "
+                        "(strong scaling) instead of one replica per rank (weak scaling)")
     p.add_argument("--no-gqa", action="store_true",
                    help="skip the grouped-query (group-shared selection) measurement")
     p.add_argument("--no-reverse", action="store_true",
@@ -75,14 +79,16 @@ def dist_env():
     return rank, world, local
 
 
-def describe(wl) -> dict:
+def describe(wl, split: bool = False) -> dict:
     return {
         "workload": f"{wl.name}: {wl.note}",
         "layers": wl.layers, "heads": wl.heads, "instances": wl.layers * wl.heads * wl.num_seqs,
         "seq_lens": wl.seq_lens, "head_dim": wl.dim, "window": wl.window,
         "capacity": wl.capacity, "pool": wl.pooling, "pool_k": wl.pool_k, "dtype": wl.dtype,
         "l2": "inputs larger than L2 (K alone exceeds the 129 MB L2 every step; no flush)",
-        "parallelism": "one replica of the workload per GPU (weak scaling)",
+        "parallelism": ("the workload's layers split over the GPUs, one contiguous share each "
+                        "(strong scaling)" if split else
+                        "one replica of the workload per GPU (weak scaling)"),
     }
 
 
@@ -632,8 +638,19 @@ def main():
         wl.layers = args.layers
     if args.heads:
         wl.heads = args.heads
-    wl.seed = shard.rank_seed(wl.seed, rank)   # rank r's own batch (weak scaling)
-    q, k, v = wk.device_tensors(wl, dev)
+    split = args.split and world > 1
+    wl_full = wl
+    if split:
+        # strong scaling: rank r takes a contiguous share of the layers of the
+        # one workload (the same bits as those layers of the whole tensors)
+        share = shard.shard_range(wl.layers, rank, world)
+        if len(share) == 0:
+            raise SystemExit("--split needs at least one layer per rank")
+        wl = dataclasses.replace(wl, layers=len(share))
+        q, k, v = wk.device_tensors(wl_full, dev, layers=share)
+    else:
+        wl.seed = shard.rank_seed(wl.seed, rank)   # rank r's own batch (weak scaling)
+        q, k, v = wk.device_tensors(wl, dev)
     shape = api.shape_of(k, wl.offsets)
     t_out = api.kvsel_out_tokens(shape, wl.capacity)
     out_idx = torch.empty((wl.layers, t_out, wl.heads), dtype=torch.int32, device=dev)
@@ -687,8 +704,11 @@ def main():
     peak, peak_kind = measured_peak_gbs()
     achieved = score_bytes / (score_ms * 1e-3) / 1e9
     step_bytes = wl.roofline_bytes()
+    # units of the whole job: every rank's replica (weak) or the one split workload (strong)
     units = wl.head_tokens()
-    value = world * units / (ms * 1e-3)
+    job_units = wl_full.head_tokens() if split else world * units
+    job_bytes = wl_full.roofline_bytes() if split else world * step_bytes
+    value = job_units / (ms * 1e-3)
 
     # Decode-side consumer: one N(0,1) query per (layer, sequence, head) over the
     # compacted cache this step produced and over the full prompt cache.
@@ -741,7 +761,7 @@ def main():
         e2e_ms = shard.max_over_ranks(ev0.elapsed_time(ev1) / args.e2e_steps, dev)
         nbytes = lambda t: t.numel() * t.element_size()
         kept_v = out_v.numel() * out_v.element_size()   # the V rows the gather reads
-        e2e = {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": job_units / (e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "h2d_bytes_per_step": nbytes(q) + nbytes(k) + kept_v,
                "d2h_bytes_per_step": nbytes(out_idx) + nbytes(out_k) + nbytes(out_v),
@@ -776,10 +796,11 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "strong" if split else "weak",
+            "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded counter-based generator)",
-            "config": describe(wl),
-            "gbs": step_bytes / (ms * 1e-3) / 1e9 * world,
+            "config": describe(wl_full, split),
+            "gbs": job_bytes / (ms * 1e-3) / 1e9,
             "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / peak,
             "roofline": {"bound": "hbm", "kernel": SCORE_KERNELS.get(path,
                                                                      "generic scoring kernels"),

@@ -356,9 +356,18 @@ def host_tensors(wl: Workload):
     return q, k, v
 
 
-def device_tensors(wl: Workload, device, chunk: int = 1 << 26):
-    """Whole tensors generated with torch on ``device`` (same bits as host_tensors)."""
+def device_tensors(wl: Workload, device, chunk: int = 1 << 26, layers: Optional[range] = None):
+    """Whole tensors generated with torch on ``device`` (same bits as host_tensors).
+
+    ``layers`` (a contiguous range of the workload's layers, default all): only
+    those layers, with the same bits as the matching slices of the whole
+    tensors (a rank's share when one workload is split over ranks)."""
     import torch
+    if layers is None:
+        layers = range(wl.layers)
+    if layers.step != 1 or layers.start < 0 or layers.stop > wl.layers:
+        raise ValueError("layers must be a contiguous range of the workload's layers")
+    nl = len(layers)
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     tq, tkv = _tables(wl)
 
@@ -368,26 +377,31 @@ def device_tensors(wl: Workload, device, chunk: int = 1 << 26):
         return torch.from_numpy(t.copy()).to(device)
 
     def fill(shape, kind, tab):
-        n = int(np.prod(shape))
+        per_layer = int(np.prod(shape[1:]))
+        n = nl * per_layer
+        base = layers.start * per_layer        # linear index of the first element
         flat = torch.empty(n, dtype=torch.int16 if wl.dtype == "bf16" else torch.float32,
                            device=device)
         s = stream_seed(wl.seed, kind)
-        pad = (-n) % 4
-        for first in range(0, n + pad, chunk):
-            cnt = min(chunk, n + pad - first)
-            c = codes_torch(s, first, cnt, device)
+        lead = base % 4                         # codes come in groups of four elements
+        total = lead + n + (-(lead + n)) % 4
+        for first in range(0, total, chunk):
+            cnt = min(chunk, total - first)
+            c = codes_torch(s, base - lead + first, cnt, device)
             vals = tab[c]
-            take = min(cnt, n - first)
-            flat[first:first + take] = vals[:take]
+            lo = max(first, lead)
+            hi = min(first + cnt, lead + n)
+            if hi > lo:
+                flat[lo - lead:hi - lead] = vals[lo - first:hi - first]
         if wl.dtype == "bf16":
             flat = flat.view(torch.bfloat16)
-        return flat.view(shape)
+        return flat.view((nl,) + tuple(shape[1:]))
 
     tqd, tkvd = tab_t(tq), tab_t(tkv)
     q = fill(wl.q_shape(), KIND_Q, tqd)
     k = fill(wl.kv_shape(), KIND_K, tkvd)
     v = fill(wl.kv_shape(), KIND_V, tkvd)
-    for layer in range(wl.layers):
+    for li, layer in enumerate(layers):
         for b in range(wl.num_seqs):
             o = wl.offsets[b]
             for h in range(wl.heads):
@@ -395,7 +409,7 @@ def device_tensors(wl: Workload, device, chunk: int = 1 << 26):
                 if dm is not None:
                     dst = torch.from_numpy(o + dm[0]).to(device)
                     src = torch.from_numpy(o + dm[1]).to(device)
-                    k[layer, dst, h] = k[layer, src, h]
+                    k[li, dst, h] = k[li, src, h]
                 pl = _plant_rows(wl, layer, b, h)
                 if pl is not None:
                     rows = torch.from_numpy(o + pl[0]).to(device)
@@ -403,7 +417,7 @@ def device_tensors(wl: Workload, device, chunk: int = 1 << 26):
                     vals = torch.from_numpy(np.ascontiguousarray(new)).to(device)
                     if wl.dtype == "bf16":
                         vals = vals.view(torch.bfloat16)
-                    k[layer, rows, h] = vals
+                    k[li, rows, h] = vals
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 

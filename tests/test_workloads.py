@@ -36,6 +36,25 @@ def test_host_equals_torch_route(dtype):
                            d.view(torch.int16) if dtype == "bf16" else d)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_layer_ranges_match_the_whole_tensors(dtype):
+    """A rank's share of a workload split by layers has the same bits as the
+    matching slices of the whole tensors (odd element counts per layer, so the
+    shares start inside a group of four generated codes)."""
+    wl = wk.custom_workload("s", 5, 3, 6, 3, 20, dtype, "avg", 3, [41, 17, 30], 77,
+                            plant=3, dup_fraction=0.25)
+    whole = wk.device_tensors(wl, "cpu", chunk=1 << 8)
+    for rng in (range(0, 2), range(2, 5), range(1, 2), range(4, 5)):
+        part = wk.device_tensors(wl, "cpu", chunk=1 << 8, layers=rng)
+        for w, p in zip(whole, part):
+            a = w[rng.start:rng.stop]
+            assert p.shape == a.shape
+            assert torch.equal(a.view(torch.int16) if dtype == "bf16" else a,
+                               p.view(torch.int16) if dtype == "bf16" else p)
+    with pytest.raises(ValueError):
+        wk.device_tensors(wl, "cpu", layers=range(3, 6))
+
+
 def test_planted_logits_rise_by_six():
     wl = wk.custom_workload("p", 1, 2, 128, 8, 64, "bf16", "max", 5, [300], 5, plant=8)
     for h in range(2):
