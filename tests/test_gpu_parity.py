@@ -211,6 +211,34 @@ def test_select_largest_budget():
         assert got[0, :, h].tolist() == want
 
 
+def test_select_packed_ragged_batch():
+    """A ragged batch whose longest prefix needs 3-CTA clusters: the two long
+    sequences take whole clusters, the short one and the bypass one run one per
+    CTA of a packed cluster; every instance bit-exact against the oracle."""
+    a = api()
+    rng = np.random.default_rng(6)
+    H, W, C = 3, 16, 2000
+    lens = [40000, 3000, 20, 17000]
+    offs = [0] + [int(x) for x in np.cumsum(lens)]
+    pooled = (rng.random((1, H, offs[-1])) * 1e-3).astype(np.float32)
+    pooled[0, 1, ::5] = pooled[0, 1, 2]          # exact ties
+    idx = a.kvsel_select(torch.from_numpy(pooled).to(DEV), offs, H, W, C)
+    assert_ok()
+    got = idx.cpu().numpy()
+    oo = 0
+    for b, length in enumerate(lens):
+        n = min(length, C)
+        for h in range(H):
+            if length < C:
+                assert got[0, oo:oo + n, h].tolist() == list(range(length))
+            else:
+                o = offs[b]
+                want = oracle.select_from_pooled(
+                    pooled[0, h, o:o + length - W].astype(np.float64), length, W, C)
+                assert got[0, oo:oo + n, h].tolist() == want
+        oo += n
+
+
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64), ("f32", 2), ("bf16", 3)])
 def test_compact_bitexact(dtype, D):
     a = api()
