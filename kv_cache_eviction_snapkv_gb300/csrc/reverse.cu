@@ -106,6 +106,43 @@ __device__ __forceinline__ int rev_nth_item(int j) {
   const int G = gridDim.x, c = blockIdx.x;
   return j * G + ((j & 1) ? G - 1 - c : c);
 }
+
+// The maximum of one row's 64 logits of a tile (kMask: only where ok(e)), in
+// eight independent chains: the maximum does not depend on the order.
+template <bool kMask, class Ok>
+__device__ __forceinline__ float rev_tile_max(const float (&x)[64], Ok ok) {
+  float mx[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], !kMask || ok(e) ? x[e] : -INFINITY);
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// P = 2^(x c2 - m) of one row's 64 keys of a tile (kMask: 0 where !ok(e)) as
+// 32 bf16 pairs hi = bf16(P) and lo = bf16(P - hi); returns the tile's sum of
+// P, taken in four interleaved partial sums added in a fixed order.
+template <bool kMask, class Ok>
+__device__ __forceinline__ float rev_tile_p(const float (&x)[64], float c2, float m, Ok ok,
+                                            uint32_t (&hw)[32], uint32_t (&lw)[32]) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    float p0 = ex2(fmaf(x[e], c2, -m)), p1 = ex2(fmaf(x[e + 1], c2, -m));
+    if (kMask) {
+      p0 = ok(e) ? p0 : 0.f;
+      p1 = ok(e + 1) ? p1 : 0.f;
+    }
+    ls[(e >> 1) & 3] += p0 + p1;
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+    const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
+    hw[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+    lw[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+  }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 // kPos: the rows carry explicit positions (every key tile is visited and the
 // mask compares positions); otherwise the row order is the position order.
 template <bool kPos>
@@ -333,13 +370,9 @@ reverse_kernel(const __grid_constant__ RevParams R) {
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
         ++u;
-        if (tile_full(jt)) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) smax = fmaxf(smax, x[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) smax = fmaxf(smax, allowed(j0 + e) ? x[e] : -INFINITY);
-        }
+        auto ok_e = [&](int e) { return allowed(j0 + e); };
+        smax = fmaxf(smax, tile_full(jt) ? rev_tile_max<false>(x, ok_e)
+                                         : rev_tile_max<true>(x, ok_e));
       }
       // the row maximum in base-2 units, from both halves
       if (ok) ms->half_m[half][r] = smax * c2;
@@ -362,18 +395,9 @@ reverse_kernel(const __grid_constant__ RevParams R) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ms->s_free[u & 1]));
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float e0 = ex2(fmaf(x[e], c2, -m)), e1 = ex2(fmaf(x[e + 1], c2, -m));
-            const float p0 = full || allowed(j0 + e) ? e0 : 0.f;
-            const float p1 = full || allowed(j0 + e + 1) ? e1 : 0.f;
-            l += p0 + p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 l2 =
-                __floats2bfloat162_rn(p0 - __low2float(h2), p1 - __high2float(h2));
-            hw[e >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
-            lw[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
-          }
+          auto ok_e = [&](int e) { return allowed(j0 + e); };
+          l += full ? rev_tile_p<false>(x, c2, m, ok_e, hw, lw)
+                    : rev_tile_p<true>(x, c2, m, ok_e, hw, lw);
         }
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->p_free), ((uint32_t)pc & 1) ^ 1,
                                                limit, abort_flag));
@@ -454,6 +478,7 @@ reverse_kernel(const __grid_constant__ RevParams R) {
 constexpr size_t reverse_smem() {
   return 1024 + (1 + kRStages) * (size_t)kRTileBytes + sizeof(RevSmem);
 }
+static_assert(reverse_smem() <= 227 * 1024, "the Q tile and the K/V ring exceed a CTA's shared memory");
 
 }  // namespace
 
