@@ -333,7 +333,10 @@ reverse_kernel(const __grid_constant__ RevParams R) {
     auto bar_soft = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kRSoft) : "memory"); };
     int u = 0, pc = 0;                   // S products and P tiles read so far (all items)
     bool ok = true;
-    for (int j = 0, item = rev_nth_item(0); ok && item < n_items; item = rev_nth_item(++j)) {
+    // After a failed wait a warp still walks the remaining items, doing no work
+    // but taking the two barriers of each, so that every softmax warp reaches
+    // every barrier whatever its own waits returned.
+    for (int j = 0, item = rev_nth_item(0); item < n_items; item = rev_nth_item(++j)) {
       const RevItem it = rev_item<kPos>(a, item);
       const int n = it.n, i = it.i0 + r, nk = it.nk;
       // debug builds also check the row against the layer's rows
@@ -376,6 +379,7 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       }
       // the row maximum in base-2 units, from both halves
       if (ok) ms->half_m[half][r] = smax * c2;
+      else *abort_flag = 1;
       bar_soft();
       if (ok) m = fmaxf(ms->half_m[0][r], ms->half_m[1][r]);
       // pass 2: P (hi, lo) of this half in registers, then into TMEM once the
@@ -415,6 +419,7 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       }
       // the row sum from both halves (half order), then O / l
       if (ok) ms->half_l[half][r] = l;
+      else *abort_flag = 1;
       bar_soft();
       if (ok) {
         l = ms->half_l[0][r] + ms->half_l[1][r];
@@ -425,7 +430,10 @@ reverse_kernel(const __grid_constant__ RevParams R) {
       if (ok)
         ok = __all_sync(0xffffffffu,
                         mbar_wait(smem_u32(&ms->o_done), (uint32_t)j & 1, limit, abort_flag));
-      if (!ok) break;
+      if (!ok) {
+        *abort_flag = 1;
+        continue;
+      }
       tc_fence_after();
       float* out = a.out + ((it.row0 + i) * a.H + it.h) * kRD + cb;
 #pragma unroll 1
